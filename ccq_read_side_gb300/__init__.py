@@ -1,0 +1,162 @@
+"""ccq_read_side_gb300 -- CCQ linear-attention forward on GB300 (sm_103a).
+
+Thin Python binding over the C ABI in include/ccq.h.  It only marshals
+arguments (torch tensors -> device pointers, the current CUDA stream); every
+step of the computation runs in the library's CUDA kernels.  There is no CPU
+path: if the library is missing, importing the binding's functions raises.
+
+    import ccq_read_side_gb300 as ccq
+    o, state = ccq.gla_fwd(q, k, v, log_alpha, w_lambda, b_lambda)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional, Tuple
+
+import torch
+
+__all__ = ["gla_fwd", "gdn_fwd", "last_device_status", "status_string", "CcqError",
+           "library", "FLAG_L2NORM_QK", "FLAG_FP32_PATH", "STATUS"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libccq.so")
+
+FLAG_L2NORM_QK = 1
+FLAG_FP32_PATH = 2
+STATUS = {0: "CCQ_OK", 1: "CCQ_ERR_INVALID_ARG", 2: "CCQ_ERR_UNSUPPORTED", 3: "CCQ_ERR_CUDA",
+          4: "CCQ_ERR_TIMEOUT", 5: "CCQ_ERR_RANGE"}
+_DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+_lib = None
+
+
+class CcqError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)}")
+
+
+def library() -> ctypes.CDLL:
+    """Load libccq.so (built by ccq_read_side_gb300.build).  Raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CCQ CUDA library not built: {LIB_PATH} is missing "
+                           "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I = ctypes.c_void_p, ctypes.c_int
+    common_tail = [P, P, P, ctypes.c_int64, P, P, P, I, I, I, I, I, I, I, ctypes.c_uint, P]
+    lib.ccq_gla_fwd.restype = I
+    lib.ccq_gla_fwd.argtypes = [P, P, P, P, P, P, P, P, P] + common_tail
+    lib.ccq_gdn_fwd.restype = I
+    lib.ccq_gdn_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P] + common_tail
+    lib.ccq_status_string.restype = ctypes.c_char_p
+    lib.ccq_status_string.argtypes = [I]
+    lib.ccq_last_device_status.restype = I
+    lib.ccq_last_device_status.argtypes = [P]
+    _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return library().ccq_status_string(int(code)).decode()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def last_device_status(stream=None) -> int:
+    """Synchronise `stream` and return (and clear) the device status word."""
+    return library().ccq_last_device_status(_stream(stream))
+
+
+def _need(t, name, dtype=None, shape=None, dev=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if dev is not None and t.device != dev:
+        raise ValueError(f"{name} is on {t.device}, expected {dev}")
+
+
+def _fwd(backbone, q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in, S0, C0, m0, t0,
+         o, lambda_out, want_state, chunk, flags, stream):
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    dev = q.device
+    for name, t, shp in (("q", q, (B, H, T, dk)), ("k", k, (B, H, T, dk)),
+                         ("v", v, (B, H, T, dv)),
+                         ("log_alpha", log_alpha,
+                          (B, H, T, dk) if backbone == "gla" else (B, H, T))):
+        _need(t, name, dt, shp, dev)
+    if backbone == "gdn":
+        _need(beta, "beta", dt, (B, H, T), dev)
+    _need(w_lambda, "w_lambda", torch.float32, (H, dk), dev)
+    _need(b_lambda, "b_lambda", torch.float32, (H,), dev)
+    _need(lambda_in, "lambda_in", torch.float32, (B, H, T), dev)
+    _need(S0, "S0", torch.float32, (B, H, dk, dv), dev)
+    _need(C0, "C0", torch.float32, (B, H, dk, dk), dev)
+    _need(m0, "m0", torch.float32, (B, H, dk), dev)
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=dt, device=dev)
+    _need(o, "o", dt, (B, H, T, dv), dev)
+    _need(lambda_out, "lambda_out", torch.float32, (B, H, T), dev)
+    S = C = m = None
+    if want_state:
+        S = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
+        C = torch.empty((B, H, dk, dk), dtype=torch.float32, device=dev)
+        m = torch.empty((B, H, dk), dtype=torch.float32, device=dev)
+    lib = library()
+    tail = (_ptr(S0), _ptr(C0), _ptr(m0), int(t0), _ptr(S), _ptr(C), _ptr(m), B, H, T, dk, dv,
+            int(chunk), _DTYPES[dt], int(flags), _stream(stream))
+    with torch.cuda.device(dev):
+        if backbone == "gla":
+            rc = lib.ccq_gla_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(w_lambda),
+                                 _ptr(b_lambda), _ptr(lambda_in), _ptr(lambda_out), _ptr(o),
+                                 *tail)
+        else:
+            rc = lib.ccq_gdn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                 _ptr(w_lambda), _ptr(b_lambda), _ptr(lambda_in),
+                                 _ptr(lambda_out), _ptr(o), *tail)
+    if rc != 0:
+        raise CcqError(rc, f"ccq_{backbone}_fwd")
+    state = None
+    if want_state:
+        state = {"S": S, "C": C, "m": m, "t0": int(t0) + T}
+    return o, state
+
+
+def gla_fwd(q, k, v, log_alpha, w_lambda=None, b_lambda=None, *, lambda_in=None, S0=None,
+            C0=None, m0=None, t0: int = 0, o=None, lambda_out=None, want_state: bool = True,
+            chunk: int = 0, flags: int = 0, stream=None) -> Tuple[torch.Tensor, Optional[Dict]]:
+    """CCQ-GLA forward on device tensors.  Returns (o, state) where state holds
+    the final S, C, m (fp32) and the token count, or None if want_state=False.
+    Asynchronous on `stream` (default: torch's current stream)."""
+    return _fwd("gla", q, k, v, log_alpha, None, w_lambda, b_lambda, lambda_in, S0, C0, m0, t0,
+                o, lambda_out, want_state, chunk, flags, stream)
+
+
+def gdn_fwd(q, k, v, log_alpha, beta, w_lambda=None, b_lambda=None, *, lambda_in=None, S0=None,
+            C0=None, m0=None, t0: int = 0, o=None, lambda_out=None, want_state: bool = True,
+            chunk: int = 0, flags: int = 0, stream=None) -> Tuple[torch.Tensor, Optional[Dict]]:
+    """CCQ forward on the Gated DeltaNet backbone (scalar log_alpha and beta [B,H,T])."""
+    return _fwd("gdn", q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in, S0, C0, m0, t0,
+                o, lambda_out, want_state, chunk, flags, stream)

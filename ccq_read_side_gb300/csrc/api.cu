@@ -1,0 +1,117 @@
+// api.cu -- the C ABI (include/ccq.h): argument checks, kernel choice, launch,
+// and the device status word.
+#include <cstdio>
+
+#include "common.cuh"
+
+namespace ccq {
+
+// One status word per device that loaded the library.
+__device__ unsigned int g_status = 0;
+
+// Device address of g_status on the current device (host code cannot take the
+// address of a __device__ variable directly).  Resolved once per device.
+static unsigned int *status_word() {
+    static unsigned int *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned int *>(ptr);
+    }
+    return addr[dev];
+}
+
+cudaError_t launch_simt(const CcqParams &p, bool gdn, bool bf16, cudaStream_t st);
+// Tensor-core GLA path (tc_gla.cu).  Returns cudaErrorNotSupported when the
+// shape is not one it takes.
+cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st);
+bool tc_gla_supported(const CcqParams &p);
+
+static ccq_status check_common(const CcqParams &p, ccq_dtype dtype) {
+    if (!p.q || !p.k || !p.v || !p.log_alpha || !p.o) return CCQ_ERR_INVALID_ARG;
+    if (p.B < 0 || p.H < 0 || p.T < 0 || p.chunk < 0 || p.t0 < 0) return CCQ_ERR_INVALID_ARG;
+    if (!p.lambda_in && (!p.w_lambda || !p.b_lambda)) return CCQ_ERR_INVALID_ARG;
+    int given = (p.S0 != nullptr) + (p.C0 != nullptr) + (p.m0 != nullptr);
+    if (given != 0 && given != 3) return CCQ_ERR_INVALID_ARG;
+    if (given == 0 && p.t0 != 0) return CCQ_ERR_INVALID_ARG;
+    if (dtype != CCQ_DTYPE_F32 && dtype != CCQ_DTYPE_BF16) return CCQ_ERR_UNSUPPORTED;
+    if ((p.dk != 64 && p.dk != 128) || (p.dv != 64 && p.dv != 128)) return CCQ_ERR_UNSUPPORTED;
+    if (p.flags & ~(CCQ_FLAG_L2NORM_QK | CCQ_FLAG_FP32_PATH)) return CCQ_ERR_INVALID_ARG;
+    if ((long long)p.B * p.H > 0x7fffffffLL) return CCQ_ERR_UNSUPPORTED;
+    if ((long long)p.T + p.t0 > (1LL << 40)) return CCQ_ERR_UNSUPPORTED;
+    return CCQ_OK;
+}
+
+static ccq_status to_status(cudaError_t e) {
+    if (e == cudaSuccess) return CCQ_OK;
+    return CCQ_ERR_CUDA;
+}
+
+}  // namespace ccq
+
+using namespace ccq;
+
+extern "C" ccq_status ccq_gla_fwd(const void *q, const void *k, const void *v,
+                                  const void *log_alpha, const float *w_lambda,
+                                  const float *b_lambda, const float *lambda_in,
+                                  float *lambda_out, void *o, const float *S0, const float *C0,
+                                  const float *m0, int64_t t0, float *S_out, float *C_out,
+                                  float *m_out, int B, int H, int T, int dk, int dv, int chunk,
+                                  ccq_dtype dtype, unsigned flags, ccq_stream_t stream) {
+    CcqParams p{q, k, v, log_alpha, nullptr, w_lambda, b_lambda, lambda_in, lambda_out, o,
+                S0, C0, m0, (long long)t0, S_out, C_out, m_out, B, H, T, dk, dv, chunk, flags,
+                nullptr};
+    ccq_status s = check_common(p, dtype);
+    if (s != CCQ_OK) return s;
+    p.status = status_word();
+    if (!p.status) return CCQ_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const bool bf16 = dtype == CCQ_DTYPE_BF16;
+    if (bf16 && !(flags & CCQ_FLAG_FP32_PATH) && tc_gla_supported(p))
+        return to_status(launch_tc_gla(p, st));
+    return to_status(launch_simt(p, false, bf16, st));
+}
+
+extern "C" ccq_status ccq_gdn_fwd(const void *q, const void *k, const void *v,
+                                  const void *log_alpha, const void *beta,
+                                  const float *w_lambda, const float *b_lambda,
+                                  const float *lambda_in, float *lambda_out, void *o,
+                                  const float *S0, const float *C0, const float *m0,
+                                  int64_t t0, float *S_out, float *C_out, float *m_out, int B,
+                                  int H, int T, int dk, int dv, int chunk, ccq_dtype dtype,
+                                  unsigned flags, ccq_stream_t stream) {
+    CcqParams p{q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in, lambda_out, o,
+                S0, C0, m0, (long long)t0, S_out, C_out, m_out, B, H, T, dk, dv, chunk, flags,
+                nullptr};
+    ccq_status s = check_common(p, dtype);
+    if (s != CCQ_OK) return s;
+    if (!beta) return CCQ_ERR_INVALID_ARG;
+    p.status = status_word();
+    if (!p.status) return CCQ_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return to_status(launch_simt(p, true, dtype == CCQ_DTYPE_BF16, st));
+}
+
+extern "C" const char *ccq_status_string(ccq_status s) {
+    switch (s) {
+        case CCQ_OK: return "CCQ_OK";
+        case CCQ_ERR_INVALID_ARG: return "CCQ_ERR_INVALID_ARG: null or inconsistent argument";
+        case CCQ_ERR_UNSUPPORTED: return "CCQ_ERR_UNSUPPORTED: shape or dtype not supported";
+        case CCQ_ERR_CUDA: return "CCQ_ERR_CUDA: a CUDA call failed";
+        case CCQ_ERR_TIMEOUT: return "CCQ_ERR_TIMEOUT: a bounded wait in a kernel gave up";
+        case CCQ_ERR_RANGE: return "CCQ_ERR_RANGE: chunk log-decay outside the tensor-core range";
+    }
+    return "CCQ: unknown status";
+}
+
+extern "C" ccq_status ccq_last_device_status(ccq_stream_t stream) {
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return CCQ_ERR_CUDA;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_status, sizeof(v)) != cudaSuccess) return CCQ_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess)
+        return CCQ_ERR_CUDA;
+    return (ccq_status)v;
+}

@@ -1,0 +1,55 @@
+// common.cuh -- small device helpers shared by the CCQ kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ccq.h"
+
+namespace ccq {
+
+// Kernels record the first error they meet in the device status word (its
+// device address travels in CcqParams::status) with atomicCAS;
+// ccq_last_device_status reads and clears it.
+__device__ __forceinline__ void record_status(unsigned int *status, unsigned int code) {
+    atomicCAS(status, 0u, code);
+}
+
+template <typename T> struct io;
+template <> struct io<float> {
+    static __device__ __forceinline__ float load(const float *p) { return *p; }
+    static __device__ __forceinline__ void store(float *p, float x) { *p = x; }
+};
+template <> struct io<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, float x) {
+        *p = __float2bfloat16_rn(x);
+    }
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + __expf(-z)); }
+
+}  // namespace ccq
+
+// Parameters shared by every kernel (device pointers, sizes).
+struct CcqParams {
+    const void *q, *k, *v, *log_alpha, *beta;
+    const float *w_lambda, *b_lambda, *lambda_in;
+    float *lambda_out;
+    void *o;
+    const float *S0, *C0, *m0;
+    long long t0;
+    float *S_out, *C_out, *m_out;
+    int B, H, T, dk, dv, chunk;
+    unsigned flags;
+    unsigned int *status;  // device status word of the current device
+};

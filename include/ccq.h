@@ -1,0 +1,126 @@
+/*
+ * ccq.h -- C ABI of the CCQ (Curvature-Conditioned Query) linear-attention
+ * forward for GB300 (sm_103a).
+ *
+ * What the library computes (per batch b, head h, token t; S is d_k x d_v):
+ *
+ *   write (the backbone's own rule, left unchanged by CCQ -- gist.science
+ *   technical summary of 2606.01294, "Don't read everything", section 2,
+ *   "integration"):
+ *     GLA              S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T   (alpha per channel)
+ *     Gated DeltaNet   S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *   key statistics, undecayed (same summary, section 2 "mechanism": one extra
+ *   d_k x d_k matrix and one d_k vector per head; 10100.com article, "cost and
+ *   limits"):
+ *     C_t = C_{t-1} + k_t k_t^T,   m_t = m_{t-1} + k_t,   n_t = n_{t-1} + 1
+ *     Sigma_t = C_t / n_t - (m_t / n_t)(m_t / n_t)^T
+ *     (the Hessian at q = 0 of log sum_{j<=t} exp(k_j^T q): same summary,
+ *     section 2 "theory")
+ *   read (10100.com article, "method", item 1; summary section 2):
+ *     lambda_t = sigmoid(w_lambda[h] . q_t + b_lambda[h])   (one scalar per token and head)
+ *     q_clean  = q_t - lambda_t Sigma_t q_t
+ *     o_t      = S_t^T q_clean                    (the summary's o_t = S_t q_clean, S as d_v x d_k)
+ *
+ * Readings where the pages are silent: the read uses S_t after token t's
+ * write; Sigma_t includes k_t and divides by n_t (population); n counts every
+ * token seen, including a carried prefix t0; the gate sees the same q that is
+ * cleaned; no 1/sqrt(d_k) query scale is applied (fold it into q).
+ *
+ * Layouts (all row-major, contiguous, in the input dtype unless stated):
+ *   q, k        [B, H, T, dk]
+ *   v, o        [B, H, T, dv]
+ *   log_alpha   GLA: [B, H, T, dk] (log of the per-channel decay, <= 0)
+ *               GDN: [B, H, T]     (log of the scalar decay, <= 0)
+ *   beta        GDN: [B, H, T]     (write strength)
+ *   w_lambda    float32 [H, dk];  b_lambda float32 [H]
+ *   lambda_in   float32 [B, H, T] or NULL: a given lambda replaces the gate
+ *               (lambda = 0 gives the plain backbone; a constant gives the
+ *               fixed-lambda mode of the article's ablation)
+ *   lambda_out  float32 [B, H, T] or NULL: the lambda actually used
+ *   S0 / S_out  float32 [B, H, dk, dv];  C0 / C_out float32 [B, H, dk, dk];
+ *   m0 / m_out  float32 [B, H, dk]
+ *               C and m are SUMS (not means); t0 is the number of tokens the
+ *               carried state has seen.  The state after the call has seen
+ *               t0 + T tokens.
+ *
+ * Ownership and execution: every pointer is device memory owned by the
+ * caller; the library allocates nothing.  Calls are asynchronous on `stream`.
+ * An argument error is returned synchronously and launches nothing.  Errors
+ * found by a kernel while it runs (a bounded wait that gave up, a decay range
+ * the tensor-core path cannot represent) are recorded in a device status word
+ * that ccq_last_device_status() reads.  Outputs of a call that recorded a
+ * device error are unspecified.
+ *
+ * Supported shapes: dk, dv in {64, 128}; T >= 0 (any tail); B*H >= 0; the
+ * `chunk` argument is a hint (0 = library default).  dtype f32 runs the fp32
+ * CUDA-core kernel; bf16 with dk = dv = 128 runs the tcgen05 tensor-core
+ * kernel (other bf16 shapes, or the CCQ_FLAG_FP32_PATH flag, run the fp32
+ * CUDA-core kernel on the bf16 inputs).
+ */
+#ifndef CCQ_H_
+#define CCQ_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *ccq_stream_t; /* same object as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+    CCQ_OK = 0,
+    CCQ_ERR_INVALID_ARG = 1, /* null required pointer, negative size, inconsistent state args */
+    CCQ_ERR_UNSUPPORTED = 2, /* shape or dtype outside the supported set */
+    CCQ_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, attribute, map) */
+    CCQ_ERR_TIMEOUT = 4,     /* device: a bounded wait inside a kernel gave up */
+    CCQ_ERR_RANGE = 5        /* device: a chunk's cumulative log-decay exceeded the
+                                tensor-core path's exponent range (|sum| > 80) */
+} ccq_status;
+
+typedef enum { CCQ_DTYPE_F32 = 0, CCQ_DTYPE_BF16 = 1 } ccq_dtype;
+
+#define CCQ_FLAG_L2NORM_QK 1u  /* normalise q and k by 1/sqrt(|x|^2 + 1e-6) before use */
+#define CCQ_FLAG_FP32_PATH 2u  /* force the fp32 CUDA-core kernel (any dtype/shape) */
+
+/*
+ * CCQ forward on the GLA backbone (definitions above).
+ * Required: q, k, v, log_alpha, o; w_lambda and b_lambda unless lambda_in.
+ * S0, C0, m0: all NULL (zero state, t0 must be 0) or all set (t0 >= 0).
+ * S_out, C_out, m_out: each nullable.  They may alias S0/C0/m0.
+ * Returns CCQ_OK after enqueueing, or an error without launching.
+ */
+ccq_status ccq_gla_fwd(const void *q, const void *k, const void *v, const void *log_alpha,
+                       const float *w_lambda, const float *b_lambda, const float *lambda_in,
+                       float *lambda_out, void *o, const float *S0, const float *C0,
+                       const float *m0, int64_t t0, float *S_out, float *C_out, float *m_out,
+                       int B, int H, int T, int dk, int dv, int chunk, ccq_dtype dtype,
+                       unsigned flags, ccq_stream_t stream);
+
+/*
+ * CCQ forward on the Gated DeltaNet backbone: same read, write
+ * S_t = alpha_t (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T with scalar
+ * log_alpha [B,H,T] and beta [B,H,T] in the input dtype.  Other arguments as
+ * ccq_gla_fwd.
+ */
+ccq_status ccq_gdn_fwd(const void *q, const void *k, const void *v, const void *log_alpha,
+                       const void *beta, const float *w_lambda, const float *b_lambda,
+                       const float *lambda_in, float *lambda_out, void *o, const float *S0,
+                       const float *C0, const float *m0, int64_t t0, float *S_out,
+                       float *C_out, float *m_out, int B, int H, int T, int dk, int dv,
+                       int chunk, ccq_dtype dtype, unsigned flags, ccq_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *ccq_status_string(ccq_status s);
+
+/*
+ * Waits for `stream`, then returns and clears the device status word of the
+ * current device (CCQ_OK if no kernel recorded an error since the last call).
+ */
+ccq_status ccq_last_device_status(ccq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCQ_H_ */

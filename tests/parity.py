@@ -1,0 +1,86 @@
+"""Shared helpers for the GPU parity tests (CUDA path vs the fp64 oracle)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import ccq_read_side_gb300 as ccq
+import oracle
+
+# Tolerances (stated by the build target): fp32 inputs -> relative L2 <= 1e-5;
+# bf16 inputs -> RMS error <= 2e-2 of the reference RMS, fp32 state.
+TOL_F32 = 1e-5
+TOL_BF16 = 2e-2
+
+
+def to_dev(inp: dict, device="cuda") -> dict:
+    out = {}
+    for k, v in inp.items():
+        out[k] = v.to(device).contiguous() if isinstance(v, torch.Tensor) else v
+    return out
+
+
+def rel_l2(got: np.ndarray, ref: np.ndarray) -> float:
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(got - ref) / (den if den > 0 else 1.0))
+
+
+def rms_ratio(got: np.ndarray, ref: np.ndarray) -> float:
+    den = np.sqrt(np.mean(ref * ref))
+    return float(np.sqrt(np.mean((got - ref) ** 2)) / (den if den > 0 else 1.0))
+
+
+def check(got, ref, dtype: str, what: str, per_head: bool = True):
+    """Whole-tensor and per-(b,h) check at the dtype's tolerance."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    f = rel_l2 if dtype == "f32" else rms_ratio
+    tol = TOL_F32 if dtype == "f32" else TOL_BF16
+    e = f(got, ref)
+    assert e <= tol, f"{what}: error {e:.3e} > {tol:.0e}"
+    if per_head and got.ndim >= 3:
+        B, H = got.shape[:2]
+        for b in range(B):
+            for h in range(H):
+                eh = f(got[b, h], ref[b, h])
+                assert eh <= tol, f"{what}[b={b},h={h}]: error {eh:.3e} > {tol:.0e}"
+    return e
+
+
+def np64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().double().cpu().numpy()
+
+
+def run_both(backbone, inp, dtype, lambda_in=None, S0=None, C0=None, m0=None, t0=0, flags=0,
+             chunk=0, l2norm=False):
+    """Run the CUDA path and the oracle on the same inputs; return both dicts."""
+    d = to_dev(inp)
+    lam_out = torch.empty(d["q"].shape[:3], dtype=torch.float32, device="cuda")
+    dev = lambda x: None if x is None else torch.as_tensor(x, dtype=torch.float32).cuda()  # noqa
+    lin = dev(lambda_in)
+    kw = dict(lambda_in=lin, S0=dev(S0), C0=dev(C0), m0=dev(m0), t0=t0, lambda_out=lam_out,
+              flags=flags | (ccq.FLAG_L2NORM_QK if l2norm else 0), chunk=chunk)
+    if backbone == "gla":
+        o, st = ccq.gla_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["w_lambda"],
+                            d["b_lambda"], **kw)
+    else:
+        o, st = ccq.gdn_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["w_lambda"],
+                            d["b_lambda"], **kw)
+    torch.cuda.synchronize()
+    assert ccq.last_device_status() == 0
+    gpu = {"o": np64(o), "lambda": np64(lam_out), "S": np64(st["S"]), "C": np64(st["C"]),
+           "m": np64(st["m"])}
+    ref = oracle.run(backbone, inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["w_lambda"],
+                     inp["b_lambda"], beta=inp.get("beta"), lambda_in=lambda_in, S0=S0, C0=C0,
+                     m0=m0, t0=t0, l2norm=l2norm)
+    return gpu, ref
+
+
+def check_all(gpu, ref, dtype, what=""):
+    check(gpu["o"], ref["o"], dtype, what + " o")
+    np.testing.assert_allclose(gpu["lambda"], ref["lambda"], rtol=1e-5, atol=1e-6,
+                               err_msg=what + " lambda")
+    for key in ("S", "C", "m"):
+        check(gpu[key], ref[key], dtype, f"{what} {key}", per_head=False)
