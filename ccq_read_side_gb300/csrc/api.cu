@@ -30,9 +30,11 @@ cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st);
 bool tc_gla_supported(const CcqParams &p);
 
 static ccq_status check_common(const CcqParams &p, ccq_dtype dtype) {
-    if (!p.q || !p.k || !p.v || !p.log_alpha || !p.o) return CCQ_ERR_INVALID_ARG;
     if (p.B < 0 || p.H < 0 || p.T < 0 || p.chunk < 0 || p.t0 < 0) return CCQ_ERR_INVALID_ARG;
-    if (!p.lambda_in && (!p.w_lambda || !p.b_lambda)) return CCQ_ERR_INVALID_ARG;
+    // Token tensors may be NULL only when there are no tokens to read.
+    const bool has_tokens = p.T > 0 && p.B > 0 && p.H > 0;
+    if (has_tokens && (!p.q || !p.k || !p.v || !p.log_alpha || !p.o)) return CCQ_ERR_INVALID_ARG;
+    if (has_tokens && !p.lambda_in && (!p.w_lambda || !p.b_lambda)) return CCQ_ERR_INVALID_ARG;
     int given = (p.S0 != nullptr) + (p.C0 != nullptr) + (p.m0 != nullptr);
     if (given != 0 && given != 3) return CCQ_ERR_INVALID_ARG;
     if (given == 0 && p.t0 != 0) return CCQ_ERR_INVALID_ARG;
@@ -87,7 +89,7 @@ extern "C" ccq_status ccq_gdn_fwd(const void *q, const void *k, const void *v,
                 nullptr};
     ccq_status s = check_common(p, dtype);
     if (s != CCQ_OK) return s;
-    if (!beta) return CCQ_ERR_INVALID_ARG;
+    if (!beta && T > 0 && B > 0 && H > 0) return CCQ_ERR_INVALID_ARG;
     p.status = status_word();
     if (!p.status) return CCQ_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -85,7 +85,8 @@ typedef enum { CCQ_DTYPE_F32 = 0, CCQ_DTYPE_BF16 = 1 } ccq_dtype;
 
 /*
  * CCQ forward on the GLA backbone (definitions above).
- * Required: q, k, v, log_alpha, o; w_lambda and b_lambda unless lambda_in.
+ * Required when T > 0 and B*H > 0: q, k, v, log_alpha, o; w_lambda and b_lambda
+ * unless lambda_in is given.
  * S0, C0, m0: all NULL (zero state, t0 must be 0) or all set (t0 >= 0).
  * S_out, C_out, m_out: each nullable.  They may alias S0/C0/m0.
  * Returns CCQ_OK after enqueueing, or an error without launching.
