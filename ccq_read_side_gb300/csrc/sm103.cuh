@@ -65,17 +65,30 @@ __device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity)
 }
 
 // Bounded spin on one phase.  `abort` (shared flag) lets every role stop as
-// soon as any of them has given up.  Returns false on timeout or abort.
-constexpr long long kSpinLimit = 1LL << 25;  // try_wait rounds (each suspends briefly): ~seconds
+// soon as any of them has given up.  Returns false on timeout (about four
+// seconds of wall time; a healthy wait lasts microseconds) or abort.
+constexpr unsigned long long kWaitNs = 4000000000ull;
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int *abort, bool cluster_scope = false) {
-    for (long long it = 0; it < kSpinLimit; ++it) {
+    if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (unsigned it = 1;; ++it) {
         if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
-        if ((it & 255) == 255 && *abort) return false;
+        if ((it & 255u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitNs) {
+                *abort = 1;
+                return false;
+            }
+        }
     }
-    *abort = 1;
-    return false;
 }
 
 __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
@@ -242,9 +255,10 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(int r, int k, int rows) {
     return (uint32_t)((k >> 6) * rows * 128 + r * 128 + ((((k & 63) >> 3) ^ (r & 7)) << 4) +
                       ((k & 7) << 1));
 }
-// Offset of the 16-byte chunk holding columns [8c, 8c+8) of row r.
-__host__ __device__ __forceinline__ uint32_t sw128_chunk(int r, int c, int rows) {
-    return (uint32_t)((c >> 3) * rows * 128 + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// Offset of the 16-byte chunk holding columns [col, col+8) of row r
+// (col a multiple of 8).
+__host__ __device__ __forceinline__ uint32_t sw128_chunk(int r, int col, int rows) {
+    return (uint32_t)((col >> 6) * rows * 128 + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4));
 }
 
 }  // namespace sm103
