@@ -2,35 +2,36 @@
 // d_k = d_v = 128, chunks of L = 64 tokens.
 //
 // One thread-block cluster of two CTAs per (b, h).  The sequence is walked
-// chunk by chunk; the two CTAs split each chunk's work by what it depends on:
+// chunk by chunk; the two CTAs split each chunk's work by what it depends on.
 //
-//   CTA 0 ("covariance side") owns the undecayed key statistics: C (d_k x d_k,
-//   fp32, in tensor memory), m (fp32, shared memory) and the token count.
-//   Per chunk it forms the CCQ read of the gist.science summary of 2606.01294
-//   (section 2, "mechanism": q_clean = q - lambda Sigma_t q, Sigma_t the key
-//   covariance including the current token), written over the chunk:
-//       A    = Q K^T                          (tcgen05, M=64 N=64 K=128)
+//   CTA 0 ("covariance side") owns the undecayed key statistics of the CCQ
+//   read (gist.science summary of 2606.01294, section 2, "mechanism": one
+//   d_k x d_k matrix C and one d_k vector m per head, maintained by the same
+//   chunked mechanism as the backbone state).  C and m live in registers of
+//   the element-wise threads (fp32); the tensor core supplies each chunk's
+//   increment dC = K^T K.  Per chunk, with t_i the tokens seen after token i:
+//       A    = Q K^T,   [m_hi m_lo w_hi w_lo] . q_i       (tcgen05, M=64)
 //       s_i  = m0.q_i + sum_{j<=i} A_ij,   Ah_ij = [j<=i] (A_ij - s_i/t_i)
-//       P^T  = C0 Q^T + K^T Ah^T              (tcgen05, M=128 N=64, K=128 / 64)
-//       qc_i = q_i - (lambda_i / t_i) (P_i - (s_i/t_i) m0)    = q_i - lambda_i Sigma q_i
-//       C   += K^T K                          (tcgen05 into the TMEM accumulator)
-//   and scales the cleaned query by the chunk's per-channel decay,
-//   Qt = qc * exp(-E), E_ic = sum of log alpha over the chunk's tokens after i
-//   (the GLA write Diag(alpha_t) of the pages' backbone), and ships Qt^T
-//   (16 KB) to CTA 1 through distributed shared memory.
+//       P^T  = C0 Q^T + K^T Ah^T                           (tcgen05, M=128 N=64)
+//       qc_i = q_i - (lambda_i / t_i) (P_i - (s_i/t_i) m0) = q_i - lambda_i Sigma_t q_i
+//   (m and w enter the tensor core as hi + lo bf16 pairs, so m0.q and the
+//   gate logit w.q keep fp32 accuracy.)  The cleaned query is scaled by the
+//   chunk's per-channel decay, Qt = qc * exp(-E), E_ic = sum of log alpha over
+//   the chunk's tokens after i, and Qt^T (16 KB) goes to CTA 1 through
+//   distributed shared memory (asynchronous bulk copy, double-buffered).
 //
-//   CTA 1 ("GLA side") owns S (d_k x d_v, fp32, in tensor memory).  With
-//   Kh = K * exp(E) (so Qt Kh^T carries exp(B_i - B_j), B the inclusive
-//   cumulative log-decay) and Sb = Diag(exp R) S0 (R = the chunk's total
-//   log-decay):
-//       Ag   = [j<=i] Qt Kh^T                 (tcgen05, M=64 N=64 K=128)
-//       O^T  = Sb^T Qt^T + V^T Ag^T           (tcgen05, M=128 N=64, K=128 / 64)
-//       S    = Sb + Kh^T V                    (tcgen05 into the TMEM accumulator)
-//   which is o_t = S_t^T q_clean with S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T.
+//   CTA 1 ("GLA side") owns S (fp32, registers).  With Kh = K * exp(E) and
+//   Sb = Diag(exp R) S (R = the chunk's total log-decay):
+//       Ag   = [j<=i] Qt Kh^T                              (tcgen05, M=64)
+//       O^T  = Sb^T Qt^T + V^T Ag^T                        (tcgen05, M=128 N=64)
+//       dS   = Kh^T V,   S <- Sb + dS                      (tcgen05 + registers)
+//   i.e. o_t = S_t^T q_clean with S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T.
 //
-// Warp roles per CTA: warps 0-3 run the element-wise steps (one thread per
-// TMEM lane), warp 4 issues TMA loads, warp 5 issues tcgen05 MMAs.  Every
-// wait is a bounded mbarrier poll; a wait that gives up records
+// Warp roles per CTA: warps 0-7 run the element-wise steps (two threads per
+// TMEM lane, each taking half of the columns), warp 8 issues TMA loads,
+// warp 9 issues tcgen05 MMAs.  The element-wise phases are ordered so that
+// the next chunk's state-independent work fills the tensor core's latency.
+// Every wait is a bounded mbarrier poll; a wait that gives up records
 // CCQ_ERR_TIMEOUT and the CTA winds down.
 #include <cuda.h>
 
@@ -44,59 +45,78 @@ using namespace sm103;
 
 namespace tcgla {
 
-constexpr int L = 64;        // tokens per chunk
-constexpr int D = 128;       // d_k = d_v
-constexpr int NTHREADS = 192;
-constexpr uint32_t TILE = L * D * 2;  // one [64 x 128] bf16 tile = two 64x64 TMA boxes
+constexpr int L = 64;         // tokens per chunk
+constexpr int D = 128;        // d_k = d_v
+constexpr int NTHREADS = 320;
+constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr uint32_t TILE = L * D * 2;  // [64 x 128] bf16 = two 64x64 TMA boxes
 constexpr uint32_t BOX = L * 64 * 2;  // 8 KB
 
-// Shared-memory tiles (byte offsets from a 1024-aligned base).  All bf16
-// tiles use the 128-byte swizzle; see sw128_off / sw128_chunk.
+// Shared-memory tiles (byte offsets from a 1024-aligned base).  bf16 tiles
+// use the 128-byte swizzle (sw128_off / sw128_chunk).  The three input tiles
+// of a stage sit at the same offsets in both CTAs (CTA 0: Q, K, log alpha;
+// CTA 1: K, log alpha, V).
 struct CovLayout {  // CTA 0
-    static constexpr uint32_t Q = 0;              // 2 stages x [64 tok][128]
-    static constexpr uint32_t K = Q + 2 * TILE;   // 2 stages
-    static constexpr uint32_t LA = K + 2 * TILE;  // 2 stages (log alpha)
-    static constexpr uint32_t C0 = LA + 2 * TILE; // bf16 C0, K-major [128 rows][128]
-    static constexpr uint32_t AH = C0 + 32768;    // bf16 Ah [64 q][64 k]
-    static constexpr uint32_t QT = AH + 8192;     // bf16 Qt^T [128 ch][64 tok] (send buffer)
-    static constexpr uint32_t END = QT + 16384;
+    static constexpr uint32_t Q = 0;               // 2 stages x [64 tok][128]
+    static constexpr uint32_t K = Q + 2 * TILE;
+    static constexpr uint32_t LA = K + 2 * TILE;   // log alpha
+    static constexpr uint32_t C0 = LA + 2 * TILE;  // 2 x bf16 C0 snapshot, K-major [128][128]
+    static constexpr uint32_t AH = C0 + 65536;     // bf16 Ah [64 q][64 k]
+    static constexpr uint32_t DOT = AH + 8192;     // bf16 [16 rows][128]: m_hi m_lo w_hi w_lo 0..
+    static constexpr uint32_t QT = DOT + 4096;     // 2 x bf16 Qt^T [128 ch][64 tok] (send)
+    static constexpr uint32_t END = QT + 32768;
 };
 struct GlaLayout {  // CTA 1
     static constexpr uint32_t K = 0;               // 2 stages
-    static constexpr uint32_t LA = K + 2 * TILE;   // 2 stages
-    static constexpr uint32_t V = LA + 2 * TILE;   // 2 stages
-    static constexpr uint32_t KH = V + 2 * TILE;   // bf16 Kh^T [128 ch][64 tok]
-    static constexpr uint32_t SB = KH + 16384;     // bf16 Sb [128 dk rows][128 dv], MN-major
+    static constexpr uint32_t LA = K + 2 * TILE;
+    static constexpr uint32_t V = LA + 2 * TILE;
+    static constexpr uint32_t KH = V + 2 * TILE;   // 2 x bf16 Kh^T [128 ch][64 tok]
+    static constexpr uint32_t SB = KH + 32768;     // bf16 Sb [128 dk][128 dv], MN-major
     static constexpr uint32_t AG = SB + 32768;     // bf16 Ag [64 q][64 k]
     static constexpr uint32_t QTR = AG + 8192;     // 2 x Qt^T receive slots
-    static constexpr uint32_t O = QTR + 32768;     // bf16 O tile [64 tok][128] (two boxes)
+    static constexpr uint32_t O = QTR + 32768;     // bf16 O tile [64 tok][128]
     static constexpr uint32_t END = O + 16384;
 };
 constexpr uint32_t TILES_END = GlaLayout::END > CovLayout::END ? GlaLayout::END : CovLayout::END;
 
 struct Aux {
-    uint64_t full[2], empty[2];                    // TMA stages
-    uint64_t b_aqk, b_p, b_c, b_c0, b_ahat;        // CTA 0
-    uint64_t qt_empty[2];                          // CTA 0: receive slot freed by CTA 1
-    uint64_t qt_full[2];                           // CTA 1: Qt^T arrived
-    uint64_t b_ops, b_stage1, b_ag, b_o;           // CTA 1
+    uint64_t full[2], empty[2];                                                      // TMA stages
+    uint64_t aqk_full[2], p_full[2], dc_full, c0_ready, ahat_ready, qt_empty[2];     // CTA 0
+    uint64_t qt_full[2], kh_ready, sb_ready, ds_full, stage1[2], ag_ready, o_full[2];  // CTA 1
     uint32_t tmem_base;
     int abort;
-    float m[D];                                    // CTA 0: running key sum
-    float w[D];                                    // CTA 0: gate weights of this head
-    float tokA[L], tokS[L];                        // CTA 0: lambda_i/t_i, s_i/t_i
+    float tokA[L], tokS[L];   // CTA 0: lambda_i / t_i, s_i / t_i
+    float part[2][D];         // partial sums exchanged between the two column halves
 };
 constexpr size_t SMEM_BYTES = 1024 + TILES_END + sizeof(Aux);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-// TMEM columns (512 allocated)
-constexpr uint32_t C_COL = 0, AQK_COL = 128, P_COL = 256;   // CTA 0
-constexpr uint32_t S_COL = 0, AG_COL = 128, O_COL = 256;    // CTA 1
+// TMEM columns (512 allocated per CTA)
+constexpr uint32_t DC_COL = 0;  // CTA 0: dC (128 columns)
+__host__ __device__ constexpr uint32_t AQK_COL(int b) { return 128 + 96 * b; }  // A (64) + dots (16)
+__host__ __device__ constexpr uint32_t P_COL(int b) { return 320 + 64 * b; }
+constexpr uint32_t DS_COL = 0;  // CTA 1: dS (128 columns)
+__host__ __device__ constexpr uint32_t AG_COL(int b) { return 128 + 64 * b; }
+__host__ __device__ constexpr uint32_t O_COL(int b) { return 256 + 64 * b; }
 constexpr uint32_t TMEM_COLS = 512;
 
 struct Args {
     CUtensorMap mq, mk, mv, mla, mo;
     CcqParams p;
 };
+
+// Optional phase timestamps of the first cluster (instrumented builds only).
+#ifdef CCQ_TRACE_BUILD
+__device__ unsigned long long g_trace[2][3][64][12];
+#define CCQ_TRACE(role, n, ev)                                           \
+    do {                                                                 \
+        if (bh == 0 && (n) < 64) g_trace[rank][role][n][ev] = clock64(); \
+    } while (0)
+#else
+#define CCQ_TRACE(role, n, ev) \
+    do {                       \
+    } while (0)
+#endif
 
 __device__ __forceinline__ float bf16_at(const uint8_t *tile, int r, int c, int rows) {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_off(r, c, rows)));
@@ -109,29 +129,38 @@ __device__ __forceinline__ void store8(uint8_t *dst, const float (&v)[8]) {
     *reinterpret_cast<uint4 *>(dst) =
         make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]), pack2(v[6], v[7]));
 }
-__device__ __forceinline__ void unpack8(uint4 u, float (&v)[8]) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        v[2 * e] = __uint_as_float(w[e] << 16);
-        v[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-    }
+// Stores elements [j0, j0+8) of a register-resident row as 8 bf16.
+template <int N>
+__device__ __forceinline__ void store8_at(uint8_t *dst, const float (&x)[N], int j0) {
+    *reinterpret_cast<uint4 *>(dst) = make_uint4(pack2(x[j0], x[j0 + 1]), pack2(x[j0 + 2], x[j0 + 3]),
+                                                 pack2(x[j0 + 4], x[j0 + 5]), pack2(x[j0 + 6], x[j0 + 7]));
 }
-// Named barrier 1 over the 128 element-wise threads (warps 0-3) that also ORs a failure
-// flag, so every thread leaves the chunk loop together.
+__device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
+__device__ __forceinline__ void put_bf16(uint8_t *p, float x) {
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
+}
+
+// Named barrier 1 over the 256 element-wise threads (warps 0-7) that also ORs
+// a failure flag, so every thread leaves the chunk loop together.
 __device__ __forceinline__ bool epi_sync_any(bool fail) {
     uint32_t r;
     asm volatile(
         "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
-        " bar.red.or.pred po, 1, 128, pi;\n selp.u32 %0, 1, 0, po;\n}"
+        " bar.red.or.pred po, 1, 256, pi;\n selp.u32 %0, 1, 0, po;\n}"
         : "=r"(r)
         : "r"((uint32_t)fail)
         : "memory");
     return r != 0;
 }
+// Warp-uniform result of a bounded wait (tcgen05.ld needs converged warps).
+__device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile int *abort,
+                                         bool cluster_scope = false) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, cluster_scope));
+}
 
-// Instruction descriptors used below (bf16 x bf16 -> fp32).
+// Instruction descriptors (bf16 x bf16 -> fp32); K = K-major, M = MN-major.
 constexpr uint32_t ID_M64N64_KK = idesc_bf16(64, 64, 0, 0);
+constexpr uint32_t ID_M64N16_KK = idesc_bf16(64, 16, 0, 0);
 constexpr uint32_t ID_M64N64_MM = idesc_bf16(64, 64, 1, 1);
 constexpr uint32_t ID_M128N64_KK = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_M128N64_MK = idesc_bf16(128, 64, 1, 0);
@@ -142,7 +171,7 @@ constexpr uint32_t ID_M128N128_KM = idesc_bf16(128, 128, 0, 1);
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 tc_gla_kernel(const __grid_constant__ Args args) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     Aux &aux = *reinterpret_cast<Aux *>(smem + TILES_END);
     const CcqParams &p = args.p;
 
@@ -151,7 +180,6 @@ tc_gla_kernel(const __grid_constant__ Args args) {
     const int bh = blockIdx.x >> 1, h = bh % p.H;
     const int T = p.T;
     const int nch = (T + L - 1) / L;
-    const uint32_t lane_base = (uint32_t)(warp & 3) * 32u;
     volatile int *abort = &aux.abort;
 
     // ------------------------------------------------------------ set-up
@@ -160,31 +188,29 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&aux.full[s]), 1);
             mbar_init(smem_u32(&aux.empty[s]), 2);
+            mbar_init(smem_u32(&aux.aqk_full[s]), 1);
+            mbar_init(smem_u32(&aux.p_full[s]), 1);
             mbar_init(smem_u32(&aux.qt_empty[s]), 1);
             mbar_init(smem_u32(&aux.qt_full[s]), 1);
+            mbar_init(smem_u32(&aux.stage1[s]), 1);
+            mbar_init(smem_u32(&aux.o_full[s]), 1);
         }
-        mbar_init(smem_u32(&aux.b_aqk), 1);
-        mbar_init(smem_u32(&aux.b_p), 1);
-        mbar_init(smem_u32(&aux.b_c), 1);
-        mbar_init(smem_u32(&aux.b_c0), 1);
-        mbar_init(smem_u32(&aux.b_ahat), 1);
-        mbar_init(smem_u32(&aux.b_ops), 1);
-        mbar_init(smem_u32(&aux.b_stage1), 1);
-        mbar_init(smem_u32(&aux.b_ag), 1);
-        mbar_init(smem_u32(&aux.b_o), 1);
+        mbar_init(smem_u32(&aux.dc_full), 1);
+        mbar_init(smem_u32(&aux.c0_ready), 1);
+        mbar_init(smem_u32(&aux.ahat_ready), 1);
+        mbar_init(smem_u32(&aux.kh_ready), 1);
+        mbar_init(smem_u32(&aux.sb_ready), 1);
+        mbar_init(smem_u32(&aux.ds_full), 1);
+        mbar_init(smem_u32(&aux.ag_ready), 1);
         fence_mbar_init();
     }
-    if (rank == 0 && tid < D) {
-        aux.m[tid] = p.m0 ? p.m0[(size_t)bh * D + tid] : 0.f;
-        aux.w[tid] = p.lambda_in ? 0.f : p.w_lambda[(size_t)h * D + tid];
-    }
-    if (warp == 4 && lane == 0) {
+    if (warp == WARP_TMA && lane == 0) {
         prefetch_tensormap(&args.mk);
         prefetch_tensormap(&args.mla);
         prefetch_tensormap(rank == 0 ? &args.mq : &args.mv);
         if (rank == 1) prefetch_tensormap(&args.mo);
     }
-    if (warp == 5) {
+    if (warp == WARP_MMA) {
         tmem_alloc(smem_u32(&aux.tmem_base), TMEM_COLS);
         tmem_relinquish();
     }
@@ -192,465 +218,522 @@ tc_gla_kernel(const __grid_constant__ Args args) {
     cluster_sync();  // barriers of both CTAs initialised before any peer traffic
     tc_fence_after();
     const uint32_t tmem = aux.tmem_base;
-    const float b_lam = p.lambda_in ? 0.f : p.b_lambda[h];
 
-    if (rank == 0) {
-        // ============================================================ CTA 0
-        if (warp == 4) {
-            if (lane == 0) {  // ---- TMA producer: Q, K, log alpha
-                for (int n = 0; n < nch; ++n) {
-                    const int s = n & 1;
-                    if (n >= 2 && !mbar_wait(smem_u32(&aux.empty[s]), ((n >> 1) - 1) & 1, abort))
-                        break;
-                    const uint32_t fb = smem_u32(&aux.full[s]);
-                    mbar_expect_tx(fb, 3 * TILE);
-                    for (int b = 0; b < 2; ++b) {
-                        tma_load_3d(smem_u32(smem + CovLayout::Q + s * TILE + b * BOX), &args.mq,
-                                    fb, b * 64, n * L, bh);
-                        tma_load_3d(smem_u32(smem + CovLayout::K + s * TILE + b * BOX), &args.mk,
-                                    fb, b * 64, n * L, bh);
-                        tma_load_3d(smem_u32(smem + CovLayout::LA + s * TILE + b * BOX),
-                                    &args.mla, fb, b * 64, n * L, bh);
-                    }
+    // element-wise thread geometry: quadrant qd owns TMEM lanes 32qd..32qd+31,
+    // half hf takes one half of the columns
+    const int qd = warp & 3, hf = (warp >> 2) & 1;
+    const int c = qd * 32 + lane;  // channel (TMEM lane)
+    const int r = qd * 16 + lane;  // row of an M=64 accumulator (lanes 0-15)
+    const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
+
+    if (warp == WARP_TMA) {
+        // ============================================================ TMA producer
+        if (lane == 0) {
+            const CUtensorMap *m0 = rank == 0 ? &args.mq : &args.mk;
+            const CUtensorMap *m1 = rank == 0 ? &args.mk : &args.mla;
+            const CUtensorMap *m2 = rank == 0 ? &args.mla : &args.mv;
+            for (int n = 0; n < nch; ++n) {
+                const int s = n & 1;
+                if (n >= 2 && !mbar_wait(smem_u32(&aux.empty[s]), ((n >> 1) - 1) & 1, abort))
+                    break;
+                CCQ_TRACE(2, n, 0);
+                const uint32_t fb = smem_u32(&aux.full[s]);
+                mbar_expect_tx(fb, 3 * TILE);
+                for (int b = 0; b < 2; ++b) {
+                    tma_load_3d(smem_u32(smem + 0 * TILE * 2 + s * TILE + b * BOX), m0, fb,
+                                b * 64, n * L, bh);
+                    tma_load_3d(smem_u32(smem + 1 * TILE * 2 + s * TILE + b * BOX), m1, fb,
+                                b * 64, n * L, bh);
+                    tma_load_3d(smem_u32(smem + 2 * TILE * 2 + s * TILE + b * BOX), m2, fb,
+                                b * 64, n * L, bh);
                 }
             }
-            __syncwarp();
-        } else if (warp == 5) {
-            if (lane == 0) {  // ---- MMA issuer
-                for (int n = 0; n < nch; ++n) {
-                    const int s = n & 1;
-                    if (!mbar_wait(smem_u32(&aux.full[s]), (n >> 1) & 1, abort)) break;
-                    tc_fence_after();
+        }
+        __syncwarp();
+    } else if (warp == WARP_MMA) {
+        // ============================================================ MMA issuer
+        if (lane == 0) {
+            for (int n = 0; n < nch; ++n) {
+                const int s = n & 1, b = n & 1;
+                const uint32_t ph2 = (n >> 1) & 1;
+                if (rank == 0) {
                     const uint32_t sQ = smem_u32(smem + CovLayout::Q + s * TILE);
                     const uint32_t sK = smem_u32(smem + CovLayout::K + s * TILE);
-                    // A = Q K^T
+                    if (!mbar_wait(smem_u32(&aux.full[s]), ph2, abort)) break;
+                    tc_fence_after();
+                    CCQ_TRACE(1, n, 0);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        uint32_t off = (ks >> 2) * BOX + (ks & 3) * 32;
-                        mma_bf16(tmem + AQK_COL, sw128_desc(sQ + off, 0, 1024),
+                    for (int ks = 0; ks < 8; ++ks) {  // A = Q K^T
+                        const uint32_t off = (ks >> 2) * BOX + (ks & 3) * 32;
+                        mma_bf16(tmem + AQK_COL(b), sw128_desc(sQ + off, 0, 1024),
                                  sw128_desc(sK + off, 0, 1024), ID_M64N64_KK, ks > 0);
                     }
-                    mma_commit(smem_u32(&aux.b_aqk));
-                    if (!mbar_wait(smem_u32(&aux.b_c0), n & 1, abort)) break;
+                    if (!mbar_wait(smem_u32(&aux.c0_ready), n & 1, abort)) break;
                     tc_fence_after();
-                    // P^T = C0 Q^T
-                    const uint32_t sC0 = smem_u32(smem + CovLayout::C0);
+                    CCQ_TRACE(1, n, 1);
+                    const uint32_t sDOT = smem_u32(smem + CovLayout::DOT);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {
-                        mma_bf16(tmem + P_COL,
+                    for (int ks = 0; ks < 8; ++ks)  // [m_hi m_lo w_hi w_lo] . q
+                        mma_bf16(tmem + AQK_COL(b) + 64,
+                                 sw128_desc(sQ + (ks >> 2) * BOX + (ks & 3) * 32, 0, 1024),
+                                 sw128_desc(sDOT + (ks >> 2) * 2048 + (ks & 3) * 32, 0, 1024),
+                                 ID_M64N16_KK, ks > 0);
+                    mma_commit(smem_u32(&aux.aqk_full[b]));
+                    const uint32_t sC0 = smem_u32(smem + CovLayout::C0 + b * 32768);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)  // P^T = C0 Q^T
+                        mma_bf16(tmem + P_COL(b),
                                  sw128_desc(sC0 + (ks >> 2) * 16384 + (ks & 3) * 32, 0, 1024),
                                  sw128_desc(sQ + (ks >> 2) * BOX + (ks & 3) * 32, 0, 1024),
                                  ID_M128N64_KK, ks > 0);
-                    }
-                    // C += K^T K
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        uint64_t dk = sw128_desc(sK + ks * 2048, BOX, 1024);
-                        mma_bf16(tmem + C_COL, dk, dk, ID_M128N128_MM, 1);
+                    for (int ks = 0; ks < 4; ++ks) {  // dC = K^T K
+                        const uint64_t dk = sw128_desc(sK + ks * 2048, BOX, 1024);
+                        mma_bf16(tmem + DC_COL, dk, dk, ID_M128N128_MM, ks > 0);
                     }
-                    mma_commit(smem_u32(&aux.b_c));
-                    if (!mbar_wait(smem_u32(&aux.b_ahat), n & 1, abort)) break;
+                    mma_commit(smem_u32(&aux.dc_full));
+                    if (!mbar_wait(smem_u32(&aux.ahat_ready), n & 1, abort)) break;
                     tc_fence_after();
-                    // P^T += K^T Ah^T
+                    CCQ_TRACE(1, n, 2);
                     const uint32_t sAH = smem_u32(smem + CovLayout::AH);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        mma_bf16(tmem + P_COL, sw128_desc(sK + ks * 2048, BOX, 1024),
+                    for (int ks = 0; ks < 4; ++ks)  // P^T += K^T Ah^T
+                        mma_bf16(tmem + P_COL(b), sw128_desc(sK + ks * 2048, BOX, 1024),
                                  sw128_desc(sAH + ks * 32, 0, 1024), ID_M128N64_MK, 1);
-                    }
-                    mma_commit(smem_u32(&aux.b_p));
+                    mma_commit(smem_u32(&aux.p_full[b]));
                     mma_commit(smem_u32(&aux.empty[s]));
-                }
-            }
-            __syncwarp();
-        } else {
-            // ---- element-wise threads: thread c <-> TMEM lane c <-> channel c
-            const int c = tid;
-            bool fail = false;
-            for (int n = 0; n < nch && !fail; ++n) {
-                const int s = n & 1;
-                const int c0t = n * L;
-                const int Lc = min(L, T - c0t);
-                const uint8_t *sQs = smem + CovLayout::Q + s * TILE;
-                const uint8_t *sKs = smem + CovLayout::K + s * TILE;
-                const uint8_t *sLAs = smem + CovLayout::LA + s * TILE;
-
-                // ---- C0 operand (bf16) for this chunk; C accumulator initialised at n = 0
-                bool ok = true;
-                if (n > 0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&aux.b_c), (n - 1) & 1, abort));
-                    tc_fence_after();
-                }
-                if (ok) {
-#pragma unroll
-                    for (int cb = 0; cb < 4; ++cb) {
-                        uint32_t r[32];
-                        const uint32_t ta = tmem + (lane_base << 16) + C_COL + cb * 32;
-                        if (n == 0) {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                r[j] = __float_as_uint(
-                                    p.C0 ? p.C0[((size_t)bh * D + c) * D + cb * 32 + j] : 0.f);
-                            tmem_st32(ta, r);
-                        } else {
-                            tmem_ld32(ta, r);
-                            tmem_ld_wait();
-                        }
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            float v[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[8 * g + e]);
-                            store8(smem + CovLayout::C0 + sw128_chunk(c, cb * 32 + 8 * g, 128), v);
-                        }
-                    }
-                    if (n == 0) tmem_st_wait();
-                }
-                tc_fence_before();
-                fence_async_smem();
-                if (epi_sync_any(!ok)) { fail = true; break; }
-                if (tid == 0) mbar_arrive(smem_u32(&aux.b_c0));
-
-                // ---- gate, s_i, Ah (one thread per query row: lanes 0-15 of each warp)
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(smem_u32(&aux.full[s]), (n >> 1) & 1, abort) &&
-                                    mbar_wait(smem_u32(&aux.b_aqk), n & 1, abort));
-                tc_fence_after();
-                if (ok) {
-                    uint32_t a0[32], a1[32];
-                    tmem_ld32(tmem + (lane_base << 16) + AQK_COL, a0);
-                    tmem_ld32(tmem + (lane_base << 16) + AQK_COL + 32, a1);
-                    tmem_ld_wait();
-                    if (lane < 16) {
-                        const int i = (warp & 3) * 16 + lane;
-                        float mq = 0.f, wq = 0.f;
-#pragma unroll 4
-                        for (int g = 0; g < 16; ++g) {
-                            float qv[8];
-                            unpack8(*reinterpret_cast<const uint4 *>(sQs + sw128_chunk(i, 8 * g, 64)),
-                                    qv);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                mq += aux.m[8 * g + e] * qv[e];
-                                wq += aux.w[8 * g + e] * qv[e];
-                            }
-                        }
-                        float rs = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (j <= i) rs += __uint_as_float(a0[j]);
-                            if (j + 32 <= i) rs += __uint_as_float(a1[j]);
-                        }
-                        const bool valid = i < Lc;
-                        const float t = (float)(p.t0 + (long long)(c0t + i + 1));
-                        const float sdt = (mq + rs) / t;
-                        float lam = 0.f;
-                        if (valid) {
-                            size_t ti = (size_t)bh * T + c0t + i;
-                            lam = p.lambda_in ? p.lambda_in[ti] : sigmoidf_(wq + b_lam);
-                            if (p.lambda_out) p.lambda_out[ti] = lam;
-                        }
-                        aux.tokA[i] = valid ? lam / t : 0.f;
-                        aux.tokS[i] = valid ? sdt : 0.f;
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            float v[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int j = 8 * g + e;
-                                const float a = __uint_as_float(j < 32 ? a0[j & 31] : a1[j & 31]);
-                                v[e] = (valid && j <= i) ? a - sdt : 0.f;
-                            }
-                            store8(smem + CovLayout::AH + sw128_chunk(i, 8 * g, 64), v);
-                        }
-                    }
-                }
-                tc_fence_before();
-                fence_async_smem();
-                if (epi_sync_any(!ok)) { fail = true; break; }
-                if (tid == 0) mbar_arrive(smem_u32(&aux.b_ahat));
-
-                // ---- cleaned, decay-scaled query Qt^T (thread c = channel c)
-                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&aux.b_p), n & 1, abort));
-                tc_fence_after();
-                if (ok) {
-                    uint32_t p0[32], p1[32];
-                    tmem_ld32(tmem + (lane_base << 16) + P_COL, p0);
-                    tmem_ld32(tmem + (lane_base << 16) + P_COL + 32, p1);
-                    tmem_ld_wait();
-                    const float mc = aux.m[c];
-                    float E = 0.f, ksum = 0.f;
-#pragma unroll
-                    for (int g = 7; g >= 0; --g) {
-                        float v[8];
-#pragma unroll
-                        for (int e = 7; e >= 0; --e) {
-                            const int i = 8 * g + e;
-                            const float la = bf16_at(sLAs, i, c, 64);
-                            const float qv = bf16_at(sQs, i, c, 64);
-                            const float P = __uint_as_float(i < 32 ? p0[i & 31] : p1[i & 31]);
-                            const float qc = qv - aux.tokA[i] * (P - aux.tokS[i] * mc);
-                            v[e] = qc * __expf(-E);
-                            E += la;
-                            ksum += bf16_at(sKs, i, c, 64);
-                        }
-                        store8(smem + CovLayout::QT + sw128_chunk(c, 8 * g, 128), v);
-                    }
-                    if (E < -80.f) record_status(p.status, CCQ_ERR_RANGE);
-                    aux.m[c] = mc + ksum;
-                }
-                fence_async_smem();
-                if (epi_sync_any(!ok)) { fail = true; break; }
-                if (tid == 0) {
-                    mbar_arrive(smem_u32(&aux.empty[s]));
-                    const int slot = n & 1;
-                    bool sent = true;
-                    if (n >= 2)
-                        sent = mbar_wait(smem_u32(&aux.qt_empty[slot]), ((n >> 1) - 1) & 1, abort,
-                                         true);
-                    if (sent) {
-                        const uint32_t rfull = mapa(smem_u32(&aux.qt_full[slot]), 1);
-                        const uint32_t rdst =
-                            mapa(smem_u32(smem + GlaLayout::QTR + slot * 16384), 1);
-                        mbar_expect_tx_cluster(rfull, 16384);
-                        bulk_copy_to_peer(rdst, smem_u32(smem + CovLayout::QT), 16384, rfull);
-                        bulk_commit();
-                        bulk_wait_read0();
-                    } else {
-                        *abort = 1;
-                    }
-                }
-            }
-            // ---- final state: C (TMEM) and m
-            if (!fail && nch > 0) {
-                bool ok = __all_sync(0xffffffffu,
-                                     mbar_wait(smem_u32(&aux.b_c), (nch - 1) & 1, abort));
-                tc_fence_after();
-                if (ok && p.C_out) {
-#pragma unroll
-                    for (int cb = 0; cb < 4; ++cb) {
-                        uint32_t r[32];
-                        tmem_ld32(tmem + (lane_base << 16) + C_COL + cb * 32, r);
-                        tmem_ld_wait();
-                        float4 *dst = reinterpret_cast<float4 *>(
-                            p.C_out + ((size_t)bh * D + c) * D + cb * 32);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                 __uint_as_float(r[4 * j + 2]),
-                                                 __uint_as_float(r[4 * j + 3]));
-                    }
-                }
-                epi_sync_any(false);
-                if (ok && p.m_out) p.m_out[(size_t)bh * D + c] = aux.m[c];
-            }
-        }
-    } else {
-        // ============================================================ CTA 1
-        if (warp == 4) {
-            if (lane == 0) {  // ---- TMA producer: K, log alpha, V
-                for (int n = 0; n < nch; ++n) {
-                    const int s = n & 1;
-                    if (n >= 2 && !mbar_wait(smem_u32(&aux.empty[s]), ((n >> 1) - 1) & 1, abort))
-                        break;
-                    const uint32_t fb = smem_u32(&aux.full[s]);
-                    mbar_expect_tx(fb, 3 * TILE);
-                    for (int b = 0; b < 2; ++b) {
-                        tma_load_3d(smem_u32(smem + GlaLayout::K + s * TILE + b * BOX), &args.mk,
-                                    fb, b * 64, n * L, bh);
-                        tma_load_3d(smem_u32(smem + GlaLayout::LA + s * TILE + b * BOX),
-                                    &args.mla, fb, b * 64, n * L, bh);
-                        tma_load_3d(smem_u32(smem + GlaLayout::V + s * TILE + b * BOX), &args.mv,
-                                    fb, b * 64, n * L, bh);
-                    }
-                }
-            }
-            __syncwarp();
-        } else if (warp == 5) {
-            if (lane == 0) {  // ---- MMA issuer
-                for (int n = 0; n < nch; ++n) {
-                    const int s = n & 1, slot = n & 1;
-                    if (!mbar_wait(smem_u32(&aux.full[s]), (n >> 1) & 1, abort)) break;
-                    if (!mbar_wait(smem_u32(&aux.b_ops), n & 1, abort)) break;
-                    if (!mbar_wait(smem_u32(&aux.qt_full[slot]), (n >> 1) & 1, abort, true)) break;
-                    tc_fence_after();
-                    const uint32_t sQT = smem_u32(smem + GlaLayout::QTR + slot * 16384);
-                    const uint32_t sKH = smem_u32(smem + GlaLayout::KH);
-                    const uint32_t sSB = smem_u32(smem + GlaLayout::SB);
+                    CCQ_TRACE(1, n, 3);
+                } else {
                     const uint32_t sV = smem_u32(smem + GlaLayout::V + s * TILE);
+                    const uint32_t sKH = smem_u32(smem + GlaLayout::KH + b * 16384);
+                    const uint32_t sSB = smem_u32(smem + GlaLayout::SB);
                     const uint32_t sAG = smem_u32(smem + GlaLayout::AG);
-                    // Ag = Qt Kh^T   (both operands stored channel-major)
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16(tmem + AG_COL, sw128_desc(sQT + ks * 2048, 16384, 1024),
-                                 sw128_desc(sKH + ks * 2048, 16384, 1024), ID_M64N64_MM, ks > 0);
-                    // O^T = Sb^T Qt^T
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)
-                        mma_bf16(tmem + O_COL, sw128_desc(sSB + ks * 2048, 16384, 1024),
-                                 sw128_desc(sQT + ks * 2048, 16384, 1024), ID_M128N64_MM, ks > 0);
-                    mma_commit(smem_u32(&aux.b_stage1));
-                    // S += Kh^T V
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem + S_COL, sw128_desc(sKH + ks * 32, 0, 1024),
-                                 sw128_desc(sV + ks * 2048, BOX, 1024), ID_M128N128_KM, 1);
-                    if (!mbar_wait(smem_u32(&aux.b_ag), n & 1, abort)) break;
+                    const uint32_t sQT = smem_u32(smem + GlaLayout::QTR + b * 16384);
+                    if (!mbar_wait(smem_u32(&aux.full[s]), ph2, abort)) break;
+                    if (!mbar_wait(smem_u32(&aux.kh_ready), n & 1, abort)) break;
+                    if (!mbar_wait(smem_u32(&aux.sb_ready), n & 1, abort)) break;
+                    CCQ_TRACE(1, n, 0);
+                    if (!mbar_wait(smem_u32(&aux.qt_full[b]), ph2, abort, true)) break;
                     tc_fence_after();
-                    // O^T += V^T Ag^T
+                    CCQ_TRACE(1, n, 1);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)
-                        mma_bf16(tmem + O_COL, sw128_desc(sV + ks * 2048, BOX, 1024),
+                    for (int ks = 0; ks < 8; ++ks)  // Ag = Qt Kh^T (both stored channel-major)
+                        mma_bf16(tmem + AG_COL(b), sw128_desc(sQT + ks * 2048, 16384, 1024),
+                                 sw128_desc(sKH + ks * 2048, 16384, 1024), ID_M64N64_MM, ks > 0);
+#pragma unroll
+                    for (int ks = 0; ks < 8; ++ks)  // O^T = Sb^T Qt^T
+                        mma_bf16(tmem + O_COL(b), sw128_desc(sSB + ks * 2048, 16384, 1024),
+                                 sw128_desc(sQT + ks * 2048, 16384, 1024), ID_M128N64_MM, ks > 0);
+                    mma_commit(smem_u32(&aux.stage1[b]));
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)  // dS = Kh^T V
+                        mma_bf16(tmem + DS_COL, sw128_desc(sKH + ks * 32, 0, 1024),
+                                 sw128_desc(sV + ks * 2048, BOX, 1024), ID_M128N128_KM, ks > 0);
+                    mma_commit(smem_u32(&aux.ds_full));
+                    if (!mbar_wait(smem_u32(&aux.ag_ready), n & 1, abort)) break;
+                    tc_fence_after();
+                    CCQ_TRACE(1, n, 2);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)  // O^T += V^T Ag^T
+                        mma_bf16(tmem + O_COL(b), sw128_desc(sV + ks * 2048, BOX, 1024),
                                  sw128_desc(sAG + ks * 32, 0, 1024), ID_M128N64_MK, 1);
-                    mma_commit(smem_u32(&aux.b_o));
+                    mma_commit(smem_u32(&aux.o_full[b]));
                     mma_commit(smem_u32(&aux.empty[s]));
+                    CCQ_TRACE(1, n, 3);
                 }
             }
-            __syncwarp();
-        } else {
-            // ---- element-wise threads: thread c <-> TMEM lane c
-            const int c = tid;
-            bool fail = false;
-            for (int n = 0; n < nch && !fail; ++n) {
-                const int s = n & 1;
-                const int c0t = n * L;
-                const uint8_t *sKs = smem + GlaLayout::K + s * TILE;
-                const uint8_t *sLAs = smem + GlaLayout::LA + s * TILE;
+        }
+        __syncwarp();
+    } else if (rank == 0) {
+        // ============================================================ CTA 0 element-wise
+        float Creg[64];  // C[c][64hf .. 64hf+64)
+        float m_cur;     // m[c] at the start of the current chunk
+        bool fail = false;
+        const float b_lam = p.lambda_in ? 0.f : p.b_lambda[h];
+        uint8_t *dot = smem + CovLayout::DOT;
 
-                // ---- Kh^T = (K * exp(E))^T and gamma = exp(R); Sb = gamma * S
-                bool ok = mbar_wait(smem_u32(&aux.full[s]), (n >> 1) & 1, abort);
-                if (n > 0) ok = ok && mbar_wait(smem_u32(&aux.b_o), (n - 1) & 1, abort);
-                ok = __all_sync(0xffffffffu, ok);
+        // ---- chunk 0 operands: C0 snapshot, m / w rows of the dot-product operand
+        {
+            const float *src = p.C0 ? p.C0 + ((size_t)bh * D + c) * D + 64 * hf : nullptr;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+                const float4 v4 =
+                    src ? *reinterpret_cast<const float4 *>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                Creg[j] = v4.x;
+                Creg[j + 1] = v4.y;
+                Creg[j + 2] = v4.z;
+                Creg[j + 3] = v4.w;
+            }
+#pragma unroll
+            for (int g = 0; g < 8; ++g)
+                store8_at(smem + CovLayout::C0 + sw128_chunk(c, 64 * hf + 8 * g, 128), Creg, 8 * g);
+            m_cur = p.m0 ? p.m0[(size_t)bh * D + c] : 0.f;
+            if (hf == 0) {
+                const float w = p.lambda_in ? 0.f : p.w_lambda[(size_t)h * D + c];
+                const float mh = __bfloat162float(__float2bfloat16_rn(m_cur));
+                const float wh = __bfloat162float(__float2bfloat16_rn(w));
+                put_bf16(dot + sw128_off(0, c, 16), mh);
+                put_bf16(dot + sw128_off(1, c, 16), m_cur - mh);
+                put_bf16(dot + sw128_off(2, c, 16), wh);
+                put_bf16(dot + sw128_off(3, c, 16), w - wh);
+            } else {
+#pragma unroll
+                for (int row = 4; row < 16; ++row) put_bf16(dot + sw128_off(row, c, 16), 0.f);
+            }
+            fence_async_smem();
+            epi_sync_any(false);
+            if (tid == 0) mbar_arrive(smem_u32(&aux.c0_ready));
+        }
+
+        for (int n = 0; n < nch; ++n) {
+            const int s = n & 1, b = n & 1;
+            const uint32_t ph2 = (n >> 1) & 1;
+            const int c0t = n * L;
+            const int Lc = min(L, T - c0t);
+            const uint8_t *sQs = smem + CovLayout::Q + s * TILE;
+            const uint8_t *sKs = smem + CovLayout::K + s * TILE;
+            const uint8_t *sLAs = smem + CovLayout::LA + s * TILE;
+            const bool more = n + 1 < nch;
+            if (tid == 0) CCQ_TRACE(0, n, 0);
+
+            // ---- gate, s_i and Ah (rows in lanes 0-15; half hf takes 32 columns)
+            bool ok = wait_all(smem_u32(&aux.aqk_full[b]), ph2, abort);
+            tc_fence_after();
+            uint32_t a[32], dt[4];
+            if (ok) {
+                tmem_ld32(tl + AQK_COL(b) + 32 * hf, a);
+                tmem_ld4(tl + AQK_COL(b) + 64, dt);
+                tmem_ld_wait();
+                float rs = 0.f;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (32 * hf + j <= r) rs += u2f(a[j]);
+                if (lane < 16) aux.part[hf][r] = rs;
+            }
+            if (epi_sync_any(!ok)) { fail = true; break; }
+            if (tid == 0) CCQ_TRACE(0, n, 1);
+            if (lane < 16) {
+                const bool valid = r < Lc;
+                const float mq = u2f(dt[0]) + u2f(dt[1]);
+                const float wq = u2f(dt[2]) + u2f(dt[3]);
+                const float t = (float)(p.t0 + (long long)(c0t + r + 1));
+                const float sdt = (mq + aux.part[0][r] + aux.part[1][r]) / t;
+                if (hf == 0) {
+                    float lam = 0.f;
+                    if (valid) {
+                        const size_t ti = (size_t)bh * T + c0t + r;
+                        lam = p.lambda_in ? p.lambda_in[ti] : sigmoidf_(wq + b_lam);
+                        if (p.lambda_out) p.lambda_out[ti] = lam;
+                    }
+                    aux.tokA[r] = valid ? lam / t : 0.f;
+                    aux.tokS[r] = valid ? sdt : 0.f;
+                }
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = 32 * hf + 8 * g + e;
+                        v[e] = (valid && j <= r) ? u2f(a[8 * g + e]) - sdt : 0.f;
+                    }
+                    store8(smem + CovLayout::AH + sw128_chunk(r, 32 * hf + 8 * g, 64), v);
+                }
+            }
+            tc_fence_before();
+            fence_async_smem();
+            if (epi_sync_any(false)) { fail = true; break; }
+            if (tid == 0) {
+                mbar_arrive(smem_u32(&aux.ahat_ready));
+                CCQ_TRACE(0, n, 2);
+            }
+
+            // ---- next chunk's operands: C += dC_n (registers), C0 snapshot, m += colsum K_n
+            ok = wait_all(smem_u32(&aux.full[s]), ph2, abort);
+            if (more) ok = ok && wait_all(smem_u32(&aux.dc_full), n & 1, abort);
+            tc_fence_after();
+            if (ok) {
+                float ksum = 0.f;
+#pragma unroll 8
+                for (int i = 0; i < 32; ++i) ksum += bf16_at(sKs, 32 * hf + i, c, 64);
+                aux.part[hf][c] = ksum;
+            }
+            if (ok && more) {
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t d[32];
+                    tmem_ld32(tl + DC_COL + 64 * hf + 32 * hb, d);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) Creg[32 * hb + j] += u2f(d[j]);
+                }
+                uint8_t *c0n = smem + CovLayout::C0 + (b ^ 1) * 32768;
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    store8_at(c0n + sw128_chunk(c, 64 * hf + 8 * g, 128), Creg, 8 * g);
+            }
+            if (epi_sync_any(!ok)) { fail = true; break; }
+            const float m_next = m_cur + aux.part[0][c] + aux.part[1][c];
+            if (more && hf == 0) {
+                const float mh = __bfloat162float(__float2bfloat16_rn(m_next));
+                put_bf16(dot + sw128_off(0, c, 16), mh);
+                put_bf16(dot + sw128_off(1, c, 16), m_next - mh);
+            }
+            tc_fence_before();
+            fence_async_smem();
+            if (tid == 0) bulk_wait_read1();  // send buffer b (chunk n-2) has been read
+            if (epi_sync_any(false)) { fail = true; break; }
+            if (tid == 0) {
+                if (more) mbar_arrive(smem_u32(&aux.c0_ready));
+                CCQ_TRACE(0, n, 3);
+            }
+
+            // ---- cleaned, decay-scaled query Qt^T (thread = channel c, 32 tokens)
+            ok = wait_all(smem_u32(&aux.p_full[b]), ph2, abort);
+            tc_fence_after();
+            if (tid == 0) CCQ_TRACE(0, n, 4);
+            if (ok) {
+                uint32_t pr[32];
+                tmem_ld32(tl + P_COL(b) + 32 * hf, pr);
+                tmem_ld_wait();
+                float E = 0.f;
+                if (hf == 0) {
+#pragma unroll 8
+                    for (int i = 32; i < 64; ++i) E += bf16_at(sLAs, i, c, 64);
+                }
+                uint8_t *qt = smem + CovLayout::QT + b * 16384;
+#pragma unroll
+                for (int g = 3; g >= 0; --g) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 7; e >= 0; --e) {
+                        const int i = 32 * hf + 8 * g + e;
+                        const float la = bf16_at(sLAs, i, c, 64);
+                        const float qv = bf16_at(sQs, i, c, 64);
+                        const float qc =
+                            qv - aux.tokA[i] * (u2f(pr[8 * g + e]) - aux.tokS[i] * m_cur);
+                        v[e] = qc * __expf(-E);
+                        E += la;
+                    }
+                    store8(qt + sw128_chunk(c, 32 * hf + 8 * g, 128), v);
+                }
+                if (hf == 0 && E < -80.f) record_status(p.status, CCQ_ERR_RANGE);
+            }
+            fence_async_smem();
+            if (epi_sync_any(!ok)) { fail = true; break; }
+            if (tid == 0) {
+                CCQ_TRACE(0, n, 5);
+                mbar_arrive(smem_u32(&aux.empty[s]));
+                bool sent = true;
+                if (n >= 2)
+                    sent = mbar_wait(smem_u32(&aux.qt_empty[b]), ((n >> 1) - 1) & 1, abort, true);
+                if (sent) {
+                    const uint32_t rfull = mapa(smem_u32(&aux.qt_full[b]), 1);
+                    const uint32_t rdst = mapa(smem_u32(smem + GlaLayout::QTR + b * 16384), 1);
+                    mbar_expect_tx_cluster(rfull, 16384);
+                    bulk_copy_to_peer(rdst, smem_u32(smem + CovLayout::QT + b * 16384), 16384,
+                                      rfull);
+                    bulk_commit();
+                }
+                CCQ_TRACE(0, n, 6);
+            }
+            m_cur = m_next;
+        }
+        // ---- final state: C = C + dC_last (registers), m
+        if (!fail && nch > 0) {
+            const bool ok = wait_all(smem_u32(&aux.dc_full), (nch - 1) & 1, abort);
+            tc_fence_after();
+            if (ok && p.C_out) {
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t d[32];
+                    tmem_ld32(tl + DC_COL + 64 * hf + 32 * hb, d);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) Creg[32 * hb + j] += u2f(d[j]);
+                }
+                float4 *dst =
+                    reinterpret_cast<float4 *>(p.C_out + ((size_t)bh * D + c) * D + 64 * hf);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    dst[j] = make_float4(Creg[4 * j], Creg[4 * j + 1], Creg[4 * j + 2], Creg[4 * j + 3]);
+            }
+            if (ok && p.m_out && hf == 0) p.m_out[(size_t)bh * D + c] = m_cur;
+        }
+        if (tid == 0) bulk_wait0();
+    } else {
+        // ============================================================ CTA 1 element-wise
+        float Sreg[64];  // S[c][64hf .. 64hf+64)
+        bool fail = false;
+        {
+            const float *src = p.S0 ? p.S0 + ((size_t)bh * D + c) * D + 64 * hf : nullptr;
+#pragma unroll
+            for (int j = 0; j < 64; j += 4) {
+                const float4 v4 =
+                    src ? *reinterpret_cast<const float4 *>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+                Sreg[j] = v4.x;
+                Sreg[j + 1] = v4.y;
+                Sreg[j + 2] = v4.z;
+                Sreg[j + 3] = v4.w;
+            }
+        }
+
+        // Kh^T of chunk k and its total decay gamma = exp(R)
+        auto kh_phase = [&](int k, float &gam) -> bool {
+            const int s = k & 1;
+            const uint8_t *sKs = smem + GlaLayout::K + s * TILE;
+            const uint8_t *sLAs = smem + GlaLayout::LA + s * TILE;
+            const bool ok = wait_all(smem_u32(&aux.full[s]), (k >> 1) & 1, abort);
+            if (ok) {
+                float other = 0.f;  // log-decay sum over the other half's tokens
+#pragma unroll 8
+                for (int i = 0; i < 32; ++i) other += bf16_at(sLAs, 32 * (hf ^ 1) + i, c, 64);
+                float E = hf == 0 ? other : 0.f;
+                uint8_t *kh = smem + GlaLayout::KH + (k & 1) * 16384;
+#pragma unroll
+                for (int g = 3; g >= 0; --g) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 7; e >= 0; --e) {
+                        const int i = 32 * hf + 8 * g + e;
+                        v[e] = bf16_at(sKs, i, c, 64) * __expf(E);
+                        E += bf16_at(sLAs, i, c, 64);
+                    }
+                    store8(kh + sw128_chunk(c, 32 * hf + 8 * g, 128), v);
+                }
+                const float R = hf == 0 ? E : E + other;
+                if (hf == 0 && R < -80.f) record_status(p.status, CCQ_ERR_RANGE);
+                gam = __expf(R);
+            }
+            fence_async_smem();
+            if (epi_sync_any(!ok)) return false;
+            if (tid == 0) {
+                mbar_arrive(smem_u32(&aux.kh_ready));
+                mbar_arrive(smem_u32(&aux.empty[s]));
+            }
+            return true;
+        };
+        // Sb = gamma * (S + dS_{k-1}): the state operand of chunk k
+        auto sb_phase = [&](int k, float gam) -> bool {
+            bool ok = true;
+            if (k > 0) {
+                ok = wait_all(smem_u32(&aux.ds_full), (k - 1) & 1, abort);
                 tc_fence_after();
                 if (ok) {
-                    float E = 0.f;
 #pragma unroll
-                    for (int g = 7; g >= 0; --g) {
+                    for (int hb = 0; hb < 2; ++hb) {
+                        uint32_t d[32];
+                        tmem_ld32(tl + DS_COL + 64 * hf + 32 * hb, d);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) Sreg[32 * hb + j] += u2f(d[j]);
+                    }
+                }
+            }
+            if (ok) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) Sreg[j] *= gam;
+#pragma unroll
+                for (int g = 0; g < 8; ++g)
+                    store8_at(smem + GlaLayout::SB + sw128_chunk(c, 64 * hf + 8 * g, 128), Sreg, 8 * g);
+            }
+            tc_fence_before();
+            fence_async_smem();
+            if (epi_sync_any(!ok)) return false;
+            if (tid == 0) mbar_arrive(smem_u32(&aux.sb_ready));
+            return true;
+        };
+
+        if (nch > 0) {
+            float gam = 1.f;
+            fail = !kh_phase(0, gam) || !sb_phase(0, gam);
+        }
+        for (int n = 0; n < nch && !fail; ++n) {
+            const int b = n & 1;
+            const uint32_t ph2 = (n >> 1) & 1;
+            const int c0t = n * L;
+            if (tid == 0) CCQ_TRACE(0, n, 0);
+
+            // ---- causal mask of Ag (rows in lanes 0-15; half hf takes 32 columns)
+            bool ok = wait_all(smem_u32(&aux.stage1[b]), ph2, abort);
+            tc_fence_after();
+            if (tid == 0) CCQ_TRACE(0, n, 1);
+            if (ok) {
+                uint32_t a[32];
+                tmem_ld32(tl + AG_COL(b) + 32 * hf, a);
+                tmem_ld_wait();
+                if (lane < 16) {
+#pragma unroll
+                    for (int g = 0; g < 4; ++g) {
                         float v[8];
 #pragma unroll
-                        for (int e = 7; e >= 0; --e) {
-                            const int i = 8 * g + e;
-                            v[e] = bf16_at(sKs, i, c, 64) * __expf(E);
-                            E += bf16_at(sLAs, i, c, 64);
-                        }
-                        store8(smem + GlaLayout::KH + sw128_chunk(c, 8 * g, 128), v);
-                    }
-                    if (E < -80.f) record_status(p.status, CCQ_ERR_RANGE);
-                    const float gam = __expf(E);
-#pragma unroll
-                    for (int cb = 0; cb < 4; ++cb) {
-                        uint32_t r[32];
-                        const uint32_t ta = tmem + (lane_base << 16) + S_COL + cb * 32;
-                        if (n == 0) {
-#pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                r[j] = __float_as_uint(
-                                    p.S0 ? p.S0[((size_t)bh * D + c) * D + cb * 32 + j] : 0.f);
-                        } else {
-                            tmem_ld32(ta, r);
-                            tmem_ld_wait();
-                        }
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(gam * __uint_as_float(r[j]));
-                        tmem_st32(ta, r);
-#pragma unroll
-                        for (int g = 0; g < 4; ++g) {
-                            float v[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[8 * g + e]);
-                            store8(smem + GlaLayout::SB + sw128_chunk(c, cb * 32 + 8 * g, 128), v);
-                        }
-                    }
-                    tmem_st_wait();
-                }
-                tc_fence_before();
-                fence_async_smem();
-                if (epi_sync_any(!ok)) { fail = true; break; }
-                if (tid == 0) {
-                    mbar_arrive(smem_u32(&aux.b_ops));
-                    mbar_arrive(smem_u32(&aux.empty[s]));
-                }
-
-                // ---- causal mask of Ag (one thread per query row)
-                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&aux.b_stage1), n & 1, abort));
-                tc_fence_after();
-                if (ok) {
-                    uint32_t a0[32], a1[32];
-                    tmem_ld32(tmem + (lane_base << 16) + AG_COL, a0);
-                    tmem_ld32(tmem + (lane_base << 16) + AG_COL + 32, a1);
-                    tmem_ld_wait();
-                    if (lane < 16) {
-                        const int i = (warp & 3) * 16 + lane;
-#pragma unroll
-                        for (int g = 0; g < 8; ++g) {
-                            float v[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const int j = 8 * g + e;
-                                const float a = __uint_as_float(j < 32 ? a0[j & 31] : a1[j & 31]);
-                                v[e] = j <= i ? a : 0.f;
-                            }
-                            store8(smem + GlaLayout::AG + sw128_chunk(i, 8 * g, 64), v);
-                        }
-                    }
-                }
-                tc_fence_before();
-                fence_async_smem();
-                if (epi_sync_any(!ok)) { fail = true; break; }
-                if (tid == 0) {
-                    mbar_arrive(smem_u32(&aux.b_ag));
-                    mbar_arrive_cluster(mapa(smem_u32(&aux.qt_empty[n & 1]), 0));
-                }
-
-                // ---- output tile: O^T lane = d_v channel, columns = tokens
-                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&aux.b_o), n & 1, abort));
-                tc_fence_after();
-                if (ok) {
-                    uint32_t o0[32], o1[32];
-                    tmem_ld32(tmem + (lane_base << 16) + O_COL, o0);
-                    tmem_ld32(tmem + (lane_base << 16) + O_COL + 32, o1);
-                    tmem_ld_wait();
-                    uint8_t *sO = smem + GlaLayout::O;
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        const float x = __uint_as_float(i < 32 ? o0[i & 31] : o1[i & 31]);
-                        *reinterpret_cast<__nv_bfloat16 *>(sO + sw128_off(i, c, 64)) =
-                            __float2bfloat16_rn(x);
-                    }
-                }
-                fence_async_smem();
-                if (epi_sync_any(!ok)) { fail = true; break; }
-                if (tid == 0) {
-                    const uint32_t sO = smem_u32(smem + GlaLayout::O);
-                    tma_store_3d(&args.mo, sO, 0, c0t, bh);
-                    tma_store_3d(&args.mo, sO + BOX, 64, c0t, bh);
-                    bulk_commit();
-                    bulk_wait_read0();
-                }
-            }
-            // ---- final state S (TMEM)
-            if (!fail && nch > 0 && p.S_out) {
-                bool ok = __all_sync(0xffffffffu,
-                                     mbar_wait(smem_u32(&aux.b_o), (nch - 1) & 1, abort));
-                tc_fence_after();
-                if (ok) {
-#pragma unroll
-                    for (int cb = 0; cb < 4; ++cb) {
-                        uint32_t r[32];
-                        tmem_ld32(tmem + (lane_base << 16) + S_COL + cb * 32, r);
-                        tmem_ld_wait();
-                        float4 *dst = reinterpret_cast<float4 *>(
-                            p.S_out + ((size_t)bh * D + c) * D + cb * 32);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                 __uint_as_float(r[4 * j + 2]),
-                                                 __uint_as_float(r[4 * j + 3]));
+                        for (int e = 0; e < 8; ++e)
+                            v[e] = (32 * hf + 8 * g + e <= r) ? u2f(a[8 * g + e]) : 0.f;
+                        store8(smem + GlaLayout::AG + sw128_chunk(r, 32 * hf + 8 * g, 64), v);
                     }
                 }
             }
-            if (tid == 0) bulk_wait0();
+            tc_fence_before();
+            fence_async_smem();
+            if (tid == 0) bulk_wait_read0();  // the O staging tile (chunk n-1) has been read
+            if (epi_sync_any(!ok)) { fail = true; break; }
+            if (tid == 0) {
+                mbar_arrive(smem_u32(&aux.ag_ready));
+                mbar_arrive_cluster(mapa(smem_u32(&aux.qt_empty[b]), 0));
+                CCQ_TRACE(0, n, 2);
+            }
+
+            // ---- next chunk's Kh^T (fills the tensor core's latency)
+            float gam_next = 1.f;
+            if (n + 1 < nch && !kh_phase(n + 1, gam_next)) { fail = true; break; }
+            if (tid == 0) CCQ_TRACE(0, n, 3);
+
+            // ---- output tile (O^T: lane = d_v channel, columns = tokens)
+            ok = wait_all(smem_u32(&aux.o_full[b]), ph2, abort);
+            tc_fence_after();
+            if (tid == 0) CCQ_TRACE(0, n, 4);
+            if (ok) {
+                uint32_t o[32];
+                tmem_ld32(tl + O_COL(b) + 32 * hf, o);
+                tmem_ld_wait();
+                uint8_t *sO = smem + GlaLayout::O;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) put_bf16(sO + sw128_off(32 * hf + j, c, 64), u2f(o[j]));
+            }
+            tc_fence_before();
+            fence_async_smem();
+            if (epi_sync_any(!ok)) { fail = true; break; }
+            if (tid == 0) {
+                const uint32_t sO = smem_u32(smem + GlaLayout::O);
+                tma_store_3d(&args.mo, sO, 0, c0t, bh);
+                tma_store_3d(&args.mo, sO + BOX, 64, c0t, bh);
+                bulk_commit();
+                CCQ_TRACE(0, n, 5);
+            }
+
+            // ---- next chunk's Sb snapshot
+            if (n + 1 < nch && !sb_phase(n + 1, gam_next)) { fail = true; break; }
         }
+        // ---- final state S = Sb_last + dS_last
+        if (!fail && nch > 0 && p.S_out) {
+            const bool ok = wait_all(smem_u32(&aux.ds_full), (nch - 1) & 1, abort);
+            tc_fence_after();
+            if (ok) {
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t d[32];
+                    tmem_ld32(tl + DS_COL + 64 * hf + 32 * hb, d);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) Sreg[32 * hb + j] += u2f(d[j]);
+                }
+                float4 *dst =
+                    reinterpret_cast<float4 *>(p.S_out + ((size_t)bh * D + c) * D + 64 * hf);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    dst[j] = make_float4(Sreg[4 * j], Sreg[4 * j + 1], Sreg[4 * j + 2], Sreg[4 * j + 3]);
+            }
+        }
+        if (tid == 0) bulk_wait0();
     }
 
     // ------------------------------------------------------------ teardown
@@ -658,7 +741,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
     __syncthreads();
     if (tid == 0 && aux.abort) record_status(p.status, CCQ_ERR_TIMEOUT);
     cluster_sync();  // no peer traffic may target a CTA that has exited
-    if (warp == 5) {
+    if (warp == WARP_MMA) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
@@ -716,9 +799,18 @@ cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st) {
         !make_map(&a.mv, p.v, p.T, BH) || !make_map(&a.mla, p.log_alpha, p.T, BH) ||
         !make_map(&a.mo, p.o, p.T, BH))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(tc_gla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    // The dynamic shared-memory limit is a per-device function attribute.
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    static bool attr_set[64] = {};
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(tc_gla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
     tc_gla_kernel<<<2 * BH, NTHREADS, SMEM_BYTES, st>>>(a);
     return cudaGetLastError();
 }
