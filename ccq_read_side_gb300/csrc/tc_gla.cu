@@ -20,6 +20,12 @@
 //   the chunk's tokens after i, and Qt^T (16 KB) goes to CTA 1 through
 //   distributed shared memory (asynchronous bulk copy, double-buffered).
 //
+//   Column-wise quantities that the element-wise threads (one per channel)
+//   would otherwise gather one bf16 at a time also come from the tensor core,
+//   exactly (bf16 inputs, fp32 accumulation): the suffix sums E^T = LA^T U^T
+//   with U the strictly-upper ones matrix (plus a ones row for the chunk total
+//   R), Q^T and K^T through an identity, and colsum(K) through a ones row.
+//
 //   CTA 1 ("GLA side") owns S (fp32, registers).  With Kh = K * exp(E) and
 //   Sb = Diag(exp R) S (R = the chunk's total log-decay):
 //       Ag   = [j<=i] Qt Kh^T                              (tcgen05, M=64)
@@ -64,40 +70,54 @@ struct CovLayout {  // CTA 0
     static constexpr uint32_t AH = C0 + 65536;     // bf16 Ah [64 q][64 k]
     static constexpr uint32_t DOT = AH + 8192;     // bf16 [16 rows][128]: m_hi m_lo w_hi w_lo 0..
     static constexpr uint32_t QT = DOT + 4096;     // 2 x bf16 Qt^T [128 ch][64 tok] (send)
-    static constexpr uint32_t END = QT + 32768;
+    static constexpr uint32_t UX = QT + 32768;     // constant U operand (see below)
+    static constexpr uint32_t ID = UX + 10240;     // constant 64x64 identity
+    static constexpr uint32_t END = ID + 8192;
 };
 struct GlaLayout {  // CTA 1
     static constexpr uint32_t K = 0;               // 2 stages
     static constexpr uint32_t LA = K + 2 * TILE;
     static constexpr uint32_t V = LA + 2 * TILE;
-    static constexpr uint32_t KH = V + 2 * TILE;   // 2 x bf16 Kh^T [128 ch][64 tok]
-    static constexpr uint32_t SB = KH + 32768;     // bf16 Sb [128 dk][128 dv], MN-major
+    static constexpr uint32_t KH = V + 2 * TILE;   // bf16 Kh^T [128 ch][64 tok]
+    static constexpr uint32_t SB = KH + 16384;     // bf16 Sb [128 dk][128 dv], MN-major
     static constexpr uint32_t AG = SB + 32768;     // bf16 Ag [64 q][64 k]
     static constexpr uint32_t QTR = AG + 8192;     // 2 x Qt^T receive slots
     static constexpr uint32_t O = QTR + 32768;     // bf16 O tile [64 tok][128]
-    static constexpr uint32_t END = O + 16384;
+    static constexpr uint32_t UX = O + 16384;
+    static constexpr uint32_t ID = UX + 10240;
+    static constexpr uint32_t END = ID + 8192;
 };
 constexpr uint32_t TILES_END = GlaLayout::END > CovLayout::END ? GlaLayout::END : CovLayout::END;
+// UX: K-major B operand [80 rows][64 tokens]: row i < 64 holds ones at token
+// columns i' > i (the strictly-upper ones matrix, so LA^T U^T gives the
+// exclusive suffix sums), row 64 is all ones (chunk totals / column sums),
+// rows 65-79 are zero.  ID: the 64x64 identity (Q^T, K^T into TMEM).
 
 struct Aux {
-    uint64_t full[2], empty[2];                                                      // TMA stages
-    uint64_t aqk_full[2], p_full[2], dc_full, c0_ready, ahat_ready, qt_empty[2];     // CTA 0
-    uint64_t qt_full[2], kh_ready, sb_ready, ds_full, stage1[2], ag_ready, o_full[2];  // CTA 1
+    uint64_t full[2], empty[2];                                                 // TMA stages
+    uint64_t aqk_full, p_full[2], dc_full, c0_ready, ahat_ready, eq_full, eq_free,
+        qt_empty[2];                                                            // CTA 0
+    uint64_t qt_full[2], kh_ready, sb_ready, ds_full, stage1, ek_full, ag_ready, o_full[2];  // CTA 1
     uint32_t tmem_base;
     int abort;
-    float tokA[L], tokS[L];   // CTA 0: lambda_i / t_i, s_i / t_i
-    float part[2][D];         // partial sums exchanged between the two column halves
+    float2 tok[L];            // CTA 0: (lambda_i / t_i, s_i / t_i)
+    float part[2][L];         // CTA 0: row-sum halves
 };
 constexpr size_t SMEM_BYTES = 1024 + TILES_END + sizeof(Aux);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM columns (512 allocated per CTA)
-constexpr uint32_t DC_COL = 0;  // CTA 0: dC (128 columns)
-__host__ __device__ constexpr uint32_t AQK_COL(int b) { return 128 + 96 * b; }  // A (64) + dots (16)
-__host__ __device__ constexpr uint32_t P_COL(int b) { return 320 + 64 * b; }
-constexpr uint32_t DS_COL = 0;  // CTA 1: dS (128 columns)
-__host__ __device__ constexpr uint32_t AG_COL(int b) { return 128 + 64 * b; }
-__host__ __device__ constexpr uint32_t O_COL(int b) { return 256 + 64 * b; }
+constexpr uint32_t DC_COL = 0;     // CTA 0: dC (128)
+constexpr uint32_t AQK_COL = 128;  //        A (64) + dots (16)
+__host__ __device__ constexpr uint32_t P_COL(int b) { return 224 + 64 * b; }
+constexpr uint32_t E0_COL = 352;   //        E^T (64)
+constexpr uint32_t QT_COL = 416;   //        Q^T (64)
+constexpr uint32_t KS_COL = 480;   //        colsum(K) (16)
+constexpr uint32_t DS_COL = 0;     // CTA 1: dS (128)
+constexpr uint32_t AG_COL = 128;   //        Ag (64)
+__host__ __device__ constexpr uint32_t O_COL(int b) { return 192 + 64 * b; }
+constexpr uint32_t E1_COL = 320;   //        E^T (64) + R (16)
+constexpr uint32_t KT_COL = 400;   //        K^T (64)
 constexpr uint32_t TMEM_COLS = 512;
 
 struct Args {
@@ -167,6 +187,8 @@ constexpr uint32_t ID_M128N64_MK = idesc_bf16(128, 64, 1, 0);
 constexpr uint32_t ID_M128N64_MM = idesc_bf16(128, 64, 1, 1);
 constexpr uint32_t ID_M128N128_MM = idesc_bf16(128, 128, 1, 1);
 constexpr uint32_t ID_M128N128_KM = idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t ID_M128N80_MK = idesc_bf16(128, 80, 1, 0);
+constexpr uint32_t ID_M128N16_MK = idesc_bf16(128, 16, 1, 0);
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 tc_gla_kernel(const __grid_constant__ Args args) {
@@ -181,28 +203,45 @@ tc_gla_kernel(const __grid_constant__ Args args) {
     const int T = p.T;
     const int nch = (T + L - 1) / L;
     volatile int *abort = &aux.abort;
+    const uint32_t UXo = rank == 0 ? CovLayout::UX : GlaLayout::UX;
+    const uint32_t IDo = rank == 0 ? CovLayout::ID : GlaLayout::ID;
 
     // ------------------------------------------------------------ set-up
     if (tid == 0) {
         aux.abort = 0;
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&aux.full[s]), 1);
-            mbar_init(smem_u32(&aux.empty[s]), 2);
-            mbar_init(smem_u32(&aux.aqk_full[s]), 1);
+            mbar_init(smem_u32(&aux.empty[s]), 1);
             mbar_init(smem_u32(&aux.p_full[s]), 1);
             mbar_init(smem_u32(&aux.qt_empty[s]), 1);
             mbar_init(smem_u32(&aux.qt_full[s]), 1);
-            mbar_init(smem_u32(&aux.stage1[s]), 1);
             mbar_init(smem_u32(&aux.o_full[s]), 1);
         }
+        mbar_init(smem_u32(&aux.aqk_full), 1);
         mbar_init(smem_u32(&aux.dc_full), 1);
         mbar_init(smem_u32(&aux.c0_ready), 1);
         mbar_init(smem_u32(&aux.ahat_ready), 1);
+        mbar_init(smem_u32(&aux.eq_full), 1);
+        mbar_init(smem_u32(&aux.eq_free), 1);
         mbar_init(smem_u32(&aux.kh_ready), 1);
         mbar_init(smem_u32(&aux.sb_ready), 1);
         mbar_init(smem_u32(&aux.ds_full), 1);
+        mbar_init(smem_u32(&aux.stage1), 1);
+        mbar_init(smem_u32(&aux.ek_full), 1);
         mbar_init(smem_u32(&aux.ag_ready), 1);
         fence_mbar_init();
+    }
+    if (warp < 8) {  // constant operands U (with the ones row) and the identity
+        for (int x = tid; x < 80 * 64; x += 256) {
+            const int row = x >> 6, col = x & 63;
+            const float v = row < 64 ? (col > row ? 1.f : 0.f) : (row == 64 ? 1.f : 0.f);
+            put_bf16(smem + UXo + sw128_off(row, col, 80), v);
+        }
+        for (int x = tid; x < 64 * 64; x += 256) {
+            const int row = x >> 6, col = x & 63;
+            put_bf16(smem + IDo + sw128_off(row, col, 64), row == col ? 1.f : 0.f);
+        }
+        fence_async_smem();
     }
     if (warp == WARP_TMA && lane == 0) {
         prefetch_tensormap(&args.mk);
@@ -240,6 +279,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 const uint32_t fb = smem_u32(&aux.full[s]);
                 mbar_expect_tx(fb, 3 * TILE);
                 for (int b = 0; b < 2; ++b) {
+                    // CTA 0: Q, K, log alpha; CTA 1: K, log alpha, V (same stage offsets)
                     tma_load_3d(smem_u32(smem + 0 * TILE * 2 + s * TILE + b * BOX), m0, fb,
                                 b * 64, n * L, bh);
                     tma_load_3d(smem_u32(smem + 1 * TILE * 2 + s * TILE + b * BOX), m1, fb,
@@ -253,32 +293,49 @@ tc_gla_kernel(const __grid_constant__ Args args) {
     } else if (warp == WARP_MMA) {
         // ============================================================ MMA issuer
         if (lane == 0) {
-            for (int n = 0; n < nch; ++n) {
-                const int s = n & 1, b = n & 1;
-                const uint32_t ph2 = (n >> 1) & 1;
-                if (rank == 0) {
+            const uint32_t sUX = smem_u32(smem + UXo);
+            const uint32_t sID = smem_u32(smem + IDo);
+            if (rank == 0) {
+                for (int n = 0; n < nch; ++n) {
+                    const int s = n & 1, b = n & 1;
+                    const uint32_t ph2 = (n >> 1) & 1;
                     const uint32_t sQ = smem_u32(smem + CovLayout::Q + s * TILE);
                     const uint32_t sK = smem_u32(smem + CovLayout::K + s * TILE);
+                    const uint32_t sLA = smem_u32(smem + CovLayout::LA + s * TILE);
                     if (!mbar_wait(smem_u32(&aux.full[s]), ph2, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 0);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks) {  // A = Q K^T
                         const uint32_t off = (ks >> 2) * BOX + (ks & 3) * 32;
-                        mma_bf16(tmem + AQK_COL(b), sw128_desc(sQ + off, 0, 1024),
+                        mma_bf16(tmem + AQK_COL, sw128_desc(sQ + off, 0, 1024),
                                  sw128_desc(sK + off, 0, 1024), ID_M64N64_KK, ks > 0);
                     }
+                    if (n > 0 && !mbar_wait(smem_u32(&aux.eq_free), (n - 1) & 1, abort)) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {  // E^T = LA^T U^T, Q^T, colsum(K)
+                        const uint64_t ub = sw128_desc(sUX + ks * 32, 0, 1024);
+                        mma_bf16(tmem + E0_COL, sw128_desc(sLA + ks * 2048, BOX, 1024), ub,
+                                 ID_M128N64_MK, ks > 0);
+                        mma_bf16(tmem + QT_COL, sw128_desc(sQ + ks * 2048, BOX, 1024),
+                                 sw128_desc(sID + ks * 32, 0, 1024), ID_M128N64_MK, ks > 0);
+                        mma_bf16(tmem + KS_COL, sw128_desc(sK + ks * 2048, BOX, 1024),
+                                 sw128_desc(sUX + 64 * 128 + ks * 32, 0, 1024), ID_M128N16_MK,
+                                 ks > 0);
+                    }
+                    mma_commit(smem_u32(&aux.eq_full));
                     if (!mbar_wait(smem_u32(&aux.c0_ready), n & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 1);
                     const uint32_t sDOT = smem_u32(smem + CovLayout::DOT);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)  // [m_hi m_lo w_hi w_lo] . q
-                        mma_bf16(tmem + AQK_COL(b) + 64,
+                        mma_bf16(tmem + AQK_COL + 64,
                                  sw128_desc(sQ + (ks >> 2) * BOX + (ks & 3) * 32, 0, 1024),
                                  sw128_desc(sDOT + (ks >> 2) * 2048 + (ks & 3) * 32, 0, 1024),
                                  ID_M64N16_KK, ks > 0);
-                    mma_commit(smem_u32(&aux.aqk_full[b]));
+                    mma_commit(smem_u32(&aux.aqk_full));
                     const uint32_t sC0 = smem_u32(smem + CovLayout::C0 + b * 32768);
 #pragma unroll
                     for (int ks = 0; ks < 8; ++ks)  // P^T = C0 Q^T
@@ -303,43 +360,68 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     mma_commit(smem_u32(&aux.p_full[b]));
                     mma_commit(smem_u32(&aux.empty[s]));
                     CCQ_TRACE(1, n, 3);
-                } else {
-                    const uint32_t sV = smem_u32(smem + GlaLayout::V + s * TILE);
-                    const uint32_t sKH = smem_u32(smem + GlaLayout::KH + b * 16384);
-                    const uint32_t sSB = smem_u32(smem + GlaLayout::SB);
-                    const uint32_t sAG = smem_u32(smem + GlaLayout::AG);
-                    const uint32_t sQT = smem_u32(smem + GlaLayout::QTR + b * 16384);
-                    if (!mbar_wait(smem_u32(&aux.full[s]), ph2, abort)) break;
-                    if (!mbar_wait(smem_u32(&aux.kh_ready), n & 1, abort)) break;
-                    if (!mbar_wait(smem_u32(&aux.sb_ready), n & 1, abort)) break;
-                    CCQ_TRACE(1, n, 0);
-                    if (!mbar_wait(smem_u32(&aux.qt_full[b]), ph2, abort, true)) break;
+                }
+            } else {
+                // E^T (+ chunk totals) and K^T of chunk k into TMEM
+                auto issue_ek = [&](int k) -> bool {
+                    const int s = k & 1;
+                    if (!mbar_wait(smem_u32(&aux.full[s]), (k >> 1) & 1, abort)) return false;
                     tc_fence_after();
-                    CCQ_TRACE(1, n, 1);
+                    const uint32_t sK = smem_u32(smem + GlaLayout::K + s * TILE);
+                    const uint32_t sLA = smem_u32(smem + GlaLayout::LA + s * TILE);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)  // Ag = Qt Kh^T (both stored channel-major)
-                        mma_bf16(tmem + AG_COL(b), sw128_desc(sQT + ks * 2048, 16384, 1024),
-                                 sw128_desc(sKH + ks * 2048, 16384, 1024), ID_M64N64_MM, ks > 0);
+                    for (int ks = 0; ks < 4; ++ks) {
+                        mma_bf16(tmem + E1_COL, sw128_desc(sLA + ks * 2048, BOX, 1024),
+                                 sw128_desc(sUX + ks * 32, 0, 1024), ID_M128N80_MK, ks > 0);
+                        mma_bf16(tmem + KT_COL, sw128_desc(sK + ks * 2048, BOX, 1024),
+                                 sw128_desc(sID + ks * 32, 0, 1024), ID_M128N64_MK, ks > 0);
+                    }
+                    mma_commit(smem_u32(&aux.ek_full));
+                    return true;
+                };
+                if (nch > 0 && issue_ek(0)) {
+                    for (int n = 0; n < nch; ++n) {
+                        const int s = n & 1, b = n & 1;
+                        const uint32_t ph2 = (n >> 1) & 1;
+                        const uint32_t sV = smem_u32(smem + GlaLayout::V + s * TILE);
+                        const uint32_t sKH = smem_u32(smem + GlaLayout::KH);
+                        const uint32_t sSB = smem_u32(smem + GlaLayout::SB);
+                        const uint32_t sAG = smem_u32(smem + GlaLayout::AG);
+                        const uint32_t sQT = smem_u32(smem + GlaLayout::QTR + b * 16384);
+                        if (!mbar_wait(smem_u32(&aux.kh_ready), n & 1, abort)) break;
+                        if (!mbar_wait(smem_u32(&aux.sb_ready), n & 1, abort)) break;
+                        CCQ_TRACE(1, n, 0);
+                        if (!mbar_wait(smem_u32(&aux.qt_full[b]), ph2, abort, true)) break;
+                        tc_fence_after();
+                        CCQ_TRACE(1, n, 1);
 #pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)  // O^T = Sb^T Qt^T
-                        mma_bf16(tmem + O_COL(b), sw128_desc(sSB + ks * 2048, 16384, 1024),
-                                 sw128_desc(sQT + ks * 2048, 16384, 1024), ID_M128N64_MM, ks > 0);
-                    mma_commit(smem_u32(&aux.stage1[b]));
+                        for (int ks = 0; ks < 8; ++ks)  // Ag = Qt Kh^T (channel-major operands)
+                            mma_bf16(tmem + AG_COL, sw128_desc(sQT + ks * 2048, 16384, 1024),
+                                     sw128_desc(sKH + ks * 2048, 16384, 1024), ID_M64N64_MM,
+                                     ks > 0);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)  // dS = Kh^T V
-                        mma_bf16(tmem + DS_COL, sw128_desc(sKH + ks * 32, 0, 1024),
-                                 sw128_desc(sV + ks * 2048, BOX, 1024), ID_M128N128_KM, ks > 0);
-                    mma_commit(smem_u32(&aux.ds_full));
-                    if (!mbar_wait(smem_u32(&aux.ag_ready), n & 1, abort)) break;
-                    tc_fence_after();
-                    CCQ_TRACE(1, n, 2);
+                        for (int ks = 0; ks < 8; ++ks)  // O^T = Sb^T Qt^T
+                            mma_bf16(tmem + O_COL(b), sw128_desc(sSB + ks * 2048, 16384, 1024),
+                                     sw128_desc(sQT + ks * 2048, 16384, 1024), ID_M128N64_MM,
+                                     ks > 0);
+                        mma_commit(smem_u32(&aux.stage1));
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)  // O^T += V^T Ag^T
-                        mma_bf16(tmem + O_COL(b), sw128_desc(sV + ks * 2048, BOX, 1024),
-                                 sw128_desc(sAG + ks * 32, 0, 1024), ID_M128N64_MK, 1);
-                    mma_commit(smem_u32(&aux.o_full[b]));
-                    mma_commit(smem_u32(&aux.empty[s]));
-                    CCQ_TRACE(1, n, 3);
+                        for (int ks = 0; ks < 4; ++ks)  // dS = Kh^T V
+                            mma_bf16(tmem + DS_COL, sw128_desc(sKH + ks * 32, 0, 1024),
+                                     sw128_desc(sV + ks * 2048, BOX, 1024), ID_M128N128_KM, ks > 0);
+                        mma_commit(smem_u32(&aux.ds_full));
+                        if (n + 1 < nch && !issue_ek(n + 1)) break;
+                        if (!mbar_wait(smem_u32(&aux.ag_ready), n & 1, abort)) break;
+                        tc_fence_after();
+                        CCQ_TRACE(1, n, 2);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks)  // O^T += V^T Ag^T
+                            mma_bf16(tmem + O_COL(b), sw128_desc(sV + ks * 2048, BOX, 1024),
+                                     sw128_desc(sAG + ks * 32, 0, 1024), ID_M128N64_MK, 1);
+                        mma_commit(smem_u32(&aux.o_full[b]));
+                        mma_commit(smem_u32(&aux.empty[s]));
+                        CCQ_TRACE(1, n, 3);
+                    }
                 }
             }
         }
@@ -390,19 +472,16 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             const uint32_t ph2 = (n >> 1) & 1;
             const int c0t = n * L;
             const int Lc = min(L, T - c0t);
-            const uint8_t *sQs = smem + CovLayout::Q + s * TILE;
-            const uint8_t *sKs = smem + CovLayout::K + s * TILE;
-            const uint8_t *sLAs = smem + CovLayout::LA + s * TILE;
             const bool more = n + 1 < nch;
             if (tid == 0) CCQ_TRACE(0, n, 0);
 
             // ---- gate, s_i and Ah (rows in lanes 0-15; half hf takes 32 columns)
-            bool ok = wait_all(smem_u32(&aux.aqk_full[b]), ph2, abort);
+            bool ok = wait_all(smem_u32(&aux.aqk_full), n & 1, abort);
             tc_fence_after();
             uint32_t a[32], dt[4];
             if (ok) {
-                tmem_ld32(tl + AQK_COL(b) + 32 * hf, a);
-                tmem_ld4(tl + AQK_COL(b) + 64, dt);
+                tmem_ld32(tl + AQK_COL + 32 * hf, a);
+                tmem_ld4(tl + AQK_COL + 64, dt);
                 tmem_ld_wait();
                 float rs = 0.f;
 #pragma unroll
@@ -425,8 +504,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                         lam = p.lambda_in ? p.lambda_in[ti] : sigmoidf_(wq + b_lam);
                         if (p.lambda_out) p.lambda_out[ti] = lam;
                     }
-                    aux.tokA[r] = valid ? lam / t : 0.f;
-                    aux.tokS[r] = valid ? sdt : 0.f;
+                    aux.tok[r] = valid ? make_float2(lam / t, sdt) : make_float2(0.f, 0.f);
                 }
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
@@ -448,14 +526,15 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             }
 
             // ---- next chunk's operands: C += dC_n (registers), C0 snapshot, m += colsum K_n
-            ok = wait_all(smem_u32(&aux.full[s]), ph2, abort);
+            ok = wait_all(smem_u32(&aux.eq_full), n & 1, abort);
             if (more) ok = ok && wait_all(smem_u32(&aux.dc_full), n & 1, abort);
             tc_fence_after();
+            float m_next = m_cur;
             if (ok) {
-                float ksum = 0.f;
-#pragma unroll 8
-                for (int i = 0; i < 32; ++i) ksum += bf16_at(sKs, 32 * hf + i, c, 64);
-                aux.part[hf][c] = ksum;
+                uint32_t ks[4];
+                tmem_ld4(tl + KS_COL, ks);
+                tmem_ld_wait();
+                m_next = m_cur + u2f(ks[0]);
             }
             if (ok && more) {
 #pragma unroll
@@ -470,18 +549,16 @@ tc_gla_kernel(const __grid_constant__ Args args) {
 #pragma unroll
                 for (int g = 0; g < 8; ++g)
                     store8_at(c0n + sw128_chunk(c, 64 * hf + 8 * g, 128), Creg, 8 * g);
-            }
-            if (epi_sync_any(!ok)) { fail = true; break; }
-            const float m_next = m_cur + aux.part[0][c] + aux.part[1][c];
-            if (more && hf == 0) {
-                const float mh = __bfloat162float(__float2bfloat16_rn(m_next));
-                put_bf16(dot + sw128_off(0, c, 16), mh);
-                put_bf16(dot + sw128_off(1, c, 16), m_next - mh);
+                if (hf == 0) {
+                    const float mh = __bfloat162float(__float2bfloat16_rn(m_next));
+                    put_bf16(dot + sw128_off(0, c, 16), mh);
+                    put_bf16(dot + sw128_off(1, c, 16), m_next - mh);
+                }
             }
             tc_fence_before();
             fence_async_smem();
             if (tid == 0) bulk_wait_read1();  // send buffer b (chunk n-2) has been read
-            if (epi_sync_any(false)) { fail = true; break; }
+            if (epi_sync_any(!ok)) { fail = true; break; }
             if (tid == 0) {
                 if (more) mbar_arrive(smem_u32(&aux.c0_ready));
                 CCQ_TRACE(0, n, 3);
@@ -492,37 +569,36 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 4);
             if (ok) {
-                uint32_t pr[32];
-                tmem_ld32(tl + P_COL(b) + 32 * hf, pr);
-                tmem_ld_wait();
-                float E = 0.f;
-                if (hf == 0) {
-#pragma unroll 8
-                    for (int i = 32; i < 64; ++i) E += bf16_at(sLAs, i, c, 64);
-                }
                 uint8_t *qt = smem + CovLayout::QT + b * 16384;
 #pragma unroll
-                for (int g = 3; g >= 0; --g) {
-                    float v[8];
+                for (int sb = 0; sb < 2; ++sb) {
+                    const int i0 = 32 * hf + 16 * sb;
+                    uint32_t pr[16], er[16], qr[16];
+                    tmem_ld16(tl + P_COL(b) + i0, pr);
+                    tmem_ld16(tl + E0_COL + i0, er);
+                    tmem_ld16(tl + QT_COL + i0, qr);
+                    tmem_ld_wait();
+                    if (i0 == 0 && u2f(er[0]) < -80.f) record_status(p.status, CCQ_ERR_RANGE);
 #pragma unroll
-                    for (int e = 7; e >= 0; --e) {
-                        const int i = 32 * hf + 8 * g + e;
-                        const float la = bf16_at(sLAs, i, c, 64);
-                        const float qv = bf16_at(sQs, i, c, 64);
-                        const float qc =
-                            qv - aux.tokA[i] * (u2f(pr[8 * g + e]) - aux.tokS[i] * m_cur);
-                        v[e] = qc * __expf(-E);
-                        E += la;
+                    for (int g = 0; g < 2; ++g) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 8 * g + e;
+                            const float2 tk = aux.tok[i0 + j];
+                            const float qc = u2f(qr[j]) - tk.x * (u2f(pr[j]) - tk.y * m_cur);
+                            v[e] = qc * exp2f(-1.4426950408889634f * u2f(er[j]));
+                        }
+                        store8(qt + sw128_chunk(c, i0 + 8 * g, 128), v);
                     }
-                    store8(qt + sw128_chunk(c, 32 * hf + 8 * g, 128), v);
                 }
-                if (hf == 0 && E < -80.f) record_status(p.status, CCQ_ERR_RANGE);
             }
+            tc_fence_before();
             fence_async_smem();
             if (epi_sync_any(!ok)) { fail = true; break; }
             if (tid == 0) {
                 CCQ_TRACE(0, n, 5);
-                mbar_arrive(smem_u32(&aux.empty[s]));
+                mbar_arrive(smem_u32(&aux.eq_free));
                 bool sent = true;
                 if (n >= 2)
                     sent = mbar_wait(smem_u32(&aux.qt_empty[b]), ((n >> 1) - 1) & 1, abort, true);
@@ -577,39 +653,43 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             }
         }
 
-        // Kh^T of chunk k and its total decay gamma = exp(R)
+        // Kh^T = (K * exp(E))^T of chunk k from E^T, K^T in TMEM; gamma = exp(R)
         auto kh_phase = [&](int k, float &gam) -> bool {
-            const int s = k & 1;
-            const uint8_t *sKs = smem + GlaLayout::K + s * TILE;
-            const uint8_t *sLAs = smem + GlaLayout::LA + s * TILE;
-            const bool ok = wait_all(smem_u32(&aux.full[s]), (k >> 1) & 1, abort);
+            bool ok = wait_all(smem_u32(&aux.ek_full), k & 1, abort);
+            // Kh (single buffer) is still read by chunk k-1's dS product
+            if (k > 0) ok = ok && wait_all(smem_u32(&aux.ds_full), (k - 1) & 1, abort);
+            tc_fence_after();
             if (ok) {
-                float other = 0.f;  // log-decay sum over the other half's tokens
-#pragma unroll 8
-                for (int i = 0; i < 32; ++i) other += bf16_at(sLAs, 32 * (hf ^ 1) + i, c, 64);
-                float E = hf == 0 ? other : 0.f;
-                uint8_t *kh = smem + GlaLayout::KH + (k & 1) * 16384;
+                uint8_t *kh = smem + GlaLayout::KH;
 #pragma unroll
-                for (int g = 3; g >= 0; --g) {
-                    float v[8];
+                for (int sb = 0; sb < 2; ++sb) {
+                    const int i0 = 32 * hf + 16 * sb;
+                    uint32_t er[16], kr[16];
+                    tmem_ld16(tl + E1_COL + i0, er);
+                    tmem_ld16(tl + KT_COL + i0, kr);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int e = 7; e >= 0; --e) {
-                        const int i = 32 * hf + 8 * g + e;
-                        v[e] = bf16_at(sKs, i, c, 64) * __expf(E);
-                        E += bf16_at(sLAs, i, c, 64);
+                    for (int g = 0; g < 2; ++g) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 8 * g + e;
+                            v[e] = u2f(kr[j]) * exp2f(1.4426950408889634f * u2f(er[j]));
+                        }
+                        store8(kh + sw128_chunk(c, i0 + 8 * g, 128), v);
                     }
-                    store8(kh + sw128_chunk(c, 32 * hf + 8 * g, 128), v);
                 }
-                const float R = hf == 0 ? E : E + other;
+                uint32_t rr[4];
+                tmem_ld4(tl + E1_COL + 64, rr);
+                tmem_ld_wait();
+                const float R = u2f(rr[0]);
                 if (hf == 0 && R < -80.f) record_status(p.status, CCQ_ERR_RANGE);
-                gam = __expf(R);
+                gam = exp2f(1.4426950408889634f * R);
             }
+            tc_fence_before();
             fence_async_smem();
             if (epi_sync_any(!ok)) return false;
-            if (tid == 0) {
-                mbar_arrive(smem_u32(&aux.kh_ready));
-                mbar_arrive(smem_u32(&aux.empty[s]));
-            }
+            if (tid == 0) mbar_arrive(smem_u32(&aux.kh_ready));
             return true;
         };
         // Sb = gamma * (S + dS_{k-1}): the state operand of chunk k
@@ -654,12 +734,12 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (tid == 0) CCQ_TRACE(0, n, 0);
 
             // ---- causal mask of Ag (rows in lanes 0-15; half hf takes 32 columns)
-            bool ok = wait_all(smem_u32(&aux.stage1[b]), ph2, abort);
+            bool ok = wait_all(smem_u32(&aux.stage1), n & 1, abort);
             tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 1);
             if (ok) {
                 uint32_t a[32];
-                tmem_ld32(tl + AG_COL(b) + 32 * hf, a);
+                tmem_ld32(tl + AG_COL + 32 * hf, a);
                 tmem_ld_wait();
                 if (lane < 16) {
 #pragma unroll
@@ -692,12 +772,16 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 4);
             if (ok) {
-                uint32_t o[32];
-                tmem_ld32(tl + O_COL(b) + 32 * hf, o);
-                tmem_ld_wait();
                 uint8_t *sO = smem + GlaLayout::O;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) put_bf16(sO + sw128_off(32 * hf + j, c, 64), u2f(o[j]));
+                for (int sb = 0; sb < 2; ++sb) {
+                    uint32_t o[16];
+                    tmem_ld16(tl + O_COL(b) + 32 * hf + 16 * sb, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        put_bf16(sO + sw128_off(32 * hf + 16 * sb + j, c, 64), u2f(o[j]));
+                }
             }
             tc_fence_before();
             fence_async_smem();
