@@ -44,7 +44,10 @@ __device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t remote_bar, uint
 }
 // try_wait suspends the thread (up to the hint, in ns) until the phase
 // completes, so waiting warps do not take issue slots from working ones.
-constexpr uint32_t kSuspendHintNs = 1000000u;
+#ifndef CCQ_SUSPEND_HINT_NS
+#define CCQ_SUSPEND_HINT_NS 1000000u
+#endif
+constexpr uint32_t kSuspendHintNs = CCQ_SUSPEND_HINT_NS;
 
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     uint32_t ok;

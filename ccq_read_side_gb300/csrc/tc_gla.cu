@@ -311,8 +311,10 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                         mma_bf16(tmem + AQK_COL, sw128_desc(sQ + off, 0, 1024),
                                  sw128_desc(sK + off, 0, 1024), ID_M64N64_KK, ks > 0);
                     }
+                    CCQ_TRACE(1, n, 4);
                     if (n > 0 && !mbar_wait(smem_u32(&aux.eq_free), (n - 1) & 1, abort)) break;
                     tc_fence_after();
+                    CCQ_TRACE(1, n, 5);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {  // E^T = LA^T U^T, Q^T, colsum(K)
                         const uint64_t ub = sw128_desc(sUX + ks * 32, 0, 1024);
@@ -478,11 +480,13 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             // ---- gate, s_i and Ah (rows in lanes 0-15; half hf takes 32 columns)
             bool ok = wait_all(smem_u32(&aux.aqk_full), n & 1, abort);
             tc_fence_after();
+            if (tid == 0) CCQ_TRACE(0, n, 1);
             uint32_t a[32], dt[4];
             if (ok) {
                 tmem_ld32(tl + AQK_COL + 32 * hf, a);
                 tmem_ld4(tl + AQK_COL + 64, dt);
                 tmem_ld_wait();
+                if (tid == 0) CCQ_TRACE(0, n, 2);
                 float rs = 0.f;
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
@@ -490,7 +494,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 if (lane < 16) aux.part[hf][r] = rs;
             }
             if (epi_sync_any(!ok)) { fail = true; break; }
-            if (tid == 0) CCQ_TRACE(0, n, 1);
+            if (tid == 0) CCQ_TRACE(0, n, 3);
             if (lane < 16) {
                 const bool valid = r < Lc;
                 const float mq = u2f(dt[0]) + u2f(dt[1]);
@@ -522,19 +526,21 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (epi_sync_any(false)) { fail = true; break; }
             if (tid == 0) {
                 mbar_arrive(smem_u32(&aux.ahat_ready));
-                CCQ_TRACE(0, n, 2);
+                CCQ_TRACE(0, n, 4);
             }
 
             // ---- next chunk's operands: C += dC_n (registers), C0 snapshot, m += colsum K_n
             ok = wait_all(smem_u32(&aux.eq_full), n & 1, abort);
             if (more) ok = ok && wait_all(smem_u32(&aux.dc_full), n & 1, abort);
             tc_fence_after();
+            if (tid == 0) CCQ_TRACE(0, n, 5);
             float m_next = m_cur;
             if (ok) {
                 uint32_t ks[4];
                 tmem_ld4(tl + KS_COL, ks);
                 tmem_ld_wait();
                 m_next = m_cur + u2f(ks[0]);
+                if (tid == 0) CCQ_TRACE(0, n, 6);
             }
             if (ok && more) {
 #pragma unroll
@@ -561,13 +567,13 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (epi_sync_any(!ok)) { fail = true; break; }
             if (tid == 0) {
                 if (more) mbar_arrive(smem_u32(&aux.c0_ready));
-                CCQ_TRACE(0, n, 3);
+                CCQ_TRACE(0, n, 7);
             }
 
             // ---- cleaned, decay-scaled query Qt^T (thread = channel c, 32 tokens)
             ok = wait_all(smem_u32(&aux.p_full[b]), ph2, abort);
             tc_fence_after();
-            if (tid == 0) CCQ_TRACE(0, n, 4);
+            if (tid == 0) CCQ_TRACE(0, n, 8);
             if (ok) {
                 uint8_t *qt = smem + CovLayout::QT + b * 16384;
 #pragma unroll
@@ -578,6 +584,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     tmem_ld16(tl + E0_COL + i0, er);
                     tmem_ld16(tl + QT_COL + i0, qr);
                     tmem_ld_wait();
+                    if (tid == 0 && sb == 0) CCQ_TRACE(0, n, 9);
                     if (i0 == 0 && u2f(er[0]) < -80.f) record_status(p.status, CCQ_ERR_RANGE);
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {
@@ -597,7 +604,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             fence_async_smem();
             if (epi_sync_any(!ok)) { fail = true; break; }
             if (tid == 0) {
-                CCQ_TRACE(0, n, 5);
+                CCQ_TRACE(0, n, 10);
                 mbar_arrive(smem_u32(&aux.eq_free));
                 bool sent = true;
                 if (n >= 2)
@@ -610,7 +617,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                                       rfull);
                     bulk_commit();
                 }
-                CCQ_TRACE(0, n, 6);
+                CCQ_TRACE(0, n, 11);
             }
             m_cur = m_next;
         }
