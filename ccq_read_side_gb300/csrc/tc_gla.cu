@@ -312,21 +312,6 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                                  sw128_desc(sK + off, 0, 1024), ID_M64N64_KK, ks > 0);
                     }
                     CCQ_TRACE(1, n, 4);
-                    if (n > 0 && !mbar_wait(smem_u32(&aux.eq_free), (n - 1) & 1, abort)) break;
-                    tc_fence_after();
-                    CCQ_TRACE(1, n, 5);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {  // E^T = LA^T U^T, Q^T, colsum(K)
-                        const uint64_t ub = sw128_desc(sUX + ks * 32, 0, 1024);
-                        mma_bf16(tmem + E0_COL, sw128_desc(sLA + ks * 2048, BOX, 1024), ub,
-                                 ID_M128N64_MK, ks > 0);
-                        mma_bf16(tmem + QT_COL, sw128_desc(sQ + ks * 2048, BOX, 1024),
-                                 sw128_desc(sID + ks * 32, 0, 1024), ID_M128N64_MK, ks > 0);
-                        mma_bf16(tmem + KS_COL, sw128_desc(sK + ks * 2048, BOX, 1024),
-                                 sw128_desc(sUX + 64 * 128 + ks * 32, 0, 1024), ID_M128N16_MK,
-                                 ks > 0);
-                    }
-                    mma_commit(smem_u32(&aux.eq_full));
                     if (!mbar_wait(smem_u32(&aux.c0_ready), n & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 1);
@@ -351,6 +336,21 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                         mma_bf16(tmem + DC_COL, dk, dk, ID_M128N128_MM, ks > 0);
                     }
                     mma_commit(smem_u32(&aux.dc_full));
+                    if (n > 0 && !mbar_wait(smem_u32(&aux.eq_free), (n - 1) & 1, abort)) break;
+                    tc_fence_after();
+                    CCQ_TRACE(1, n, 5);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {  // E^T = LA^T U^T, Q^T, colsum(K)
+                        const uint64_t ub = sw128_desc(sUX + ks * 32, 0, 1024);
+                        mma_bf16(tmem + E0_COL, sw128_desc(sLA + ks * 2048, BOX, 1024), ub,
+                                 ID_M128N64_MK, ks > 0);
+                        mma_bf16(tmem + QT_COL, sw128_desc(sQ + ks * 2048, BOX, 1024),
+                                 sw128_desc(sID + ks * 32, 0, 1024), ID_M128N64_MK, ks > 0);
+                        mma_bf16(tmem + KS_COL, sw128_desc(sK + ks * 2048, BOX, 1024),
+                                 sw128_desc(sUX + 64 * 128 + ks * 32, 0, 1024), ID_M128N16_MK,
+                                 ks > 0);
+                    }
+                    mma_commit(smem_u32(&aux.eq_full));
                     if (!mbar_wait(smem_u32(&aux.ahat_ready), n & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 2);
@@ -499,16 +499,16 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 const bool valid = r < Lc;
                 const float mq = u2f(dt[0]) + u2f(dt[1]);
                 const float wq = u2f(dt[2]) + u2f(dt[3]);
-                const float t = (float)(p.t0 + (long long)(c0t + r + 1));
-                const float sdt = (mq + aux.part[0][r] + aux.part[1][r]) / t;
+                const float rt = __frcp_rn((float)(p.t0 + (long long)(c0t + r + 1)));  // 1 / t_i
+                const float sdt = (mq + aux.part[0][r] + aux.part[1][r]) * rt;
                 if (hf == 0) {
                     float lam = 0.f;
                     if (valid) {
                         const size_t ti = (size_t)bh * T + c0t + r;
-                        lam = p.lambda_in ? p.lambda_in[ti] : sigmoidf_(wq + b_lam);
+                        lam = p.lambda_in ? p.lambda_in[ti] : __frcp_rn(1.f + __expf(-(wq + b_lam)));
                         if (p.lambda_out) p.lambda_out[ti] = lam;
                     }
-                    aux.tok[r] = valid ? make_float2(lam / t, sdt) : make_float2(0.f, 0.f);
+                    aux.tok[r] = valid ? make_float2(lam * rt, sdt) : make_float2(0.f, 0.f);
                 }
 #pragma unroll
                 for (int g = 0; g < 4; ++g) {
