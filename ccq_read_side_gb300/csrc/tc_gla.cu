@@ -7,9 +7,10 @@
 //   CTA 0 ("covariance side") owns the undecayed key statistics of the CCQ
 //   read (gist.science summary of 2606.01294, section 2, "mechanism": one
 //   d_k x d_k matrix C and one d_k vector m per head, maintained by the same
-//   chunked mechanism as the backbone state).  C and m live in registers of
-//   the element-wise threads (fp32); the tensor core supplies each chunk's
-//   increment dC = K^T K.  Per chunk, with t_i the tokens seen after token i:
+//   chunked mechanism as the backbone state).  C is an fp32 accumulator in
+//   tensor memory (C += K^T K per chunk); a bf16 snapshot of it is the MMA
+//   operand of the next chunk.  m is kept in registers.  Per chunk, with t_i
+//   the number of tokens seen after token i:
 //       A    = Q K^T,   [m_hi m_lo w_hi w_lo] . q_i       (tcgen05, M=64)
 //       s_i  = m0.q_i + sum_{j<=i} A_ij,   Ah_ij = [j<=i] (A_ij - s_i/t_i)
 //       P^T  = C0 Q^T + K^T Ah^T                           (tcgen05, M=128 N=64)
@@ -20,25 +21,26 @@
 //   the chunk's tokens after i, and Qt^T (16 KB) goes to CTA 1 through
 //   distributed shared memory (asynchronous bulk copy, double-buffered).
 //
-//   Column-wise quantities that the element-wise threads (one per channel)
-//   would otherwise gather one bf16 at a time also come from the tensor core,
-//   exactly (bf16 inputs, fp32 accumulation): the suffix sums E^T = LA^T U^T
-//   with U the strictly-upper ones matrix (plus a ones row for the chunk total
-//   R), Q^T and K^T through an identity, and colsum(K) through a ones row.
+//   Column-wise quantities that the element-wise threads (one lane per
+//   channel) would otherwise gather one bf16 at a time also come from the
+//   tensor core, exactly (bf16 inputs, fp32 accumulation): the suffix sums
+//   E^T = LA^T U^T with U the strictly-upper ones matrix (plus a ones row for
+//   the chunk total R), Q^T and K^T through an identity, and colsum(K)
+//   through a ones row.
 //
-//   CTA 1 ("GLA side") owns S (fp32, registers).  With Kh = K * exp(E) and
-//   Sb = Diag(exp R) S (R = the chunk's total log-decay):
+//   CTA 1 ("GLA side") owns S (fp32 accumulator in tensor memory).  With
+//   Kh = K * exp(E) and Sb = Diag(exp R) S (R = the chunk's total log-decay):
 //       Ag   = [j<=i] Qt Kh^T                              (tcgen05, M=64)
 //       O^T  = Sb^T Qt^T + V^T Ag^T                        (tcgen05, M=128 N=64)
-//       dS   = Kh^T V,   S <- Sb + dS                      (tcgen05 + registers)
+//       S    = Sb + Kh^T V                                 (rescale in TMEM, then tcgen05)
 //   i.e. o_t = S_t^T q_clean with S_t = Diag(alpha_t) S_{t-1} + k_t v_t^T.
 //
-// Warp roles per CTA: warps 0-7 run the element-wise steps (two threads per
-// TMEM lane, each taking half of the columns), warp 8 issues TMA loads,
-// warp 9 issues tcgen05 MMAs.  The element-wise phases are ordered so that
-// the next chunk's state-independent work fills the tensor core's latency.
-// Every wait is a bounded mbarrier poll; a wait that gives up records
-// CCQ_ERR_TIMEOUT and the CTA winds down.
+// Warp roles per CTA: warps 0-15 run the element-wise steps (four threads
+// per TMEM lane, each taking a quarter of the columns), warp 16 issues TMA
+// loads, warp 17 issues tcgen05 MMAs.  The element-wise phases are ordered
+// so that the next chunk's state-independent work fills the tensor core's
+// latency.  Every wait is a bounded mbarrier poll; a wait that gives up
+// records CCQ_ERR_TIMEOUT and the CTA winds down.
 #include <cuda.h>
 
 #include <mutex>
@@ -53,8 +55,9 @@ namespace tcgla {
 
 constexpr int L = 64;         // tokens per chunk
 constexpr int D = 128;        // d_k = d_v
-constexpr int NTHREADS = 320;
-constexpr int WARP_TMA = 8, WARP_MMA = 9;
+constexpr int NEPI = 512;      // element-wise threads (warps 0-15)
+constexpr int NTHREADS = 576;
+constexpr int WARP_TMA = 16, WARP_MMA = 17;
 constexpr uint32_t TILE = L * D * 2;  // [64 x 128] bf16 = two 64x64 TMA boxes
 constexpr uint32_t BOX = L * 64 * 2;  // 8 KB
 
@@ -101,19 +104,19 @@ struct Aux {
     uint32_t tmem_base;
     int abort;
     float2 tok[L];            // CTA 0: (lambda_i / t_i, s_i / t_i)
-    float part[2][L];         // CTA 0: row-sum halves
+    float part[4][L];         // CTA 0: row-sum quarters
 };
 constexpr size_t SMEM_BYTES = 1024 + TILES_END + sizeof(Aux);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // TMEM columns (512 allocated per CTA)
-constexpr uint32_t DC_COL = 0;     // CTA 0: dC (128)
+constexpr uint32_t C_COL = 0;      // CTA 0: C accumulator (128)
 constexpr uint32_t AQK_COL = 128;  //        A (64) + dots (16)
 __host__ __device__ constexpr uint32_t P_COL(int b) { return 224 + 64 * b; }
 constexpr uint32_t E0_COL = 352;   //        E^T (64)
 constexpr uint32_t QT_COL = 416;   //        Q^T (64)
 constexpr uint32_t KS_COL = 480;   //        colsum(K) (16)
-constexpr uint32_t DS_COL = 0;     // CTA 1: dS (128)
+constexpr uint32_t S_COL = 0;      // CTA 1: S accumulator (128)
 constexpr uint32_t AG_COL = 128;   //        Ag (64)
 __host__ __device__ constexpr uint32_t O_COL(int b) { return 192 + 64 * b; }
 constexpr uint32_t E1_COL = 320;   //        E^T (64) + R (16)
@@ -160,13 +163,13 @@ __device__ __forceinline__ void put_bf16(uint8_t *p, float x) {
     *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
 }
 
-// Named barrier 1 over the 256 element-wise threads (warps 0-7) that also ORs
+// Named barrier 1 over the 512 element-wise threads (warps 0-15) that also ORs
 // a failure flag, so every thread leaves the chunk loop together.
 __device__ __forceinline__ bool epi_sync_any(bool fail) {
     uint32_t r;
     asm volatile(
         "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
-        " bar.red.or.pred po, 1, 256, pi;\n selp.u32 %0, 1, 0, po;\n}"
+        " bar.red.or.pred po, 1, 512, pi;\n selp.u32 %0, 1, 0, po;\n}"
         : "=r"(r)
         : "r"((uint32_t)fail)
         : "memory");
@@ -231,13 +234,13 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         mbar_init(smem_u32(&aux.ag_ready), 1);
         fence_mbar_init();
     }
-    if (warp < 8) {  // constant operands U (with the ones row) and the identity
-        for (int x = tid; x < 80 * 64; x += 256) {
+    if (warp < NEPI / 32) {  // constant operands U (with the ones row) and the identity
+        for (int x = tid; x < 80 * 64; x += NEPI) {
             const int row = x >> 6, col = x & 63;
             const float v = row < 64 ? (col > row ? 1.f : 0.f) : (row == 64 ? 1.f : 0.f);
             put_bf16(smem + UXo + sw128_off(row, col, 80), v);
         }
-        for (int x = tid; x < 64 * 64; x += 256) {
+        for (int x = tid; x < 64 * 64; x += NEPI) {
             const int row = x >> 6, col = x & 63;
             put_bf16(smem + IDo + sw128_off(row, col, 64), row == col ? 1.f : 0.f);
         }
@@ -259,8 +262,8 @@ tc_gla_kernel(const __grid_constant__ Args args) {
     const uint32_t tmem = aux.tmem_base;
 
     // element-wise thread geometry: quadrant qd owns TMEM lanes 32qd..32qd+31,
-    // half hf takes one half of the columns
-    const int qd = warp & 3, hf = (warp >> 2) & 1;
+    // quarter qt takes one quarter of the columns
+    const int qd = warp & 3, qt = (warp >> 2) & 3;
     const int c = qd * 32 + lane;  // channel (TMEM lane)
     const int r = qd * 16 + lane;  // row of an M=64 accumulator (lanes 0-15)
     const uint32_t tl = tmem + ((uint32_t)(qd * 32) << 16);
@@ -331,9 +334,9 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                                  sw128_desc(sQ + (ks >> 2) * BOX + (ks & 3) * 32, 0, 1024),
                                  ID_M128N64_KK, ks > 0);
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {  // dC = K^T K
+                    for (int ks = 0; ks < 4; ++ks) {  // C += K^T K
                         const uint64_t dk = sw128_desc(sK + ks * 2048, BOX, 1024);
-                        mma_bf16(tmem + DC_COL, dk, dk, ID_M128N128_MM, ks > 0);
+                        mma_bf16(tmem + C_COL, dk, dk, ID_M128N128_MM, 1);
                     }
                     mma_commit(smem_u32(&aux.dc_full));
                     if (n > 0 && !mbar_wait(smem_u32(&aux.eq_free), (n - 1) & 1, abort)) break;
@@ -408,9 +411,9 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                                      ks > 0);
                         mma_commit(smem_u32(&aux.stage1));
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)  // dS = Kh^T V
-                            mma_bf16(tmem + DS_COL, sw128_desc(sKH + ks * 32, 0, 1024),
-                                     sw128_desc(sV + ks * 2048, BOX, 1024), ID_M128N128_KM, ks > 0);
+                        for (int ks = 0; ks < 4; ++ks)  // S = Sb + Kh^T V (Sb already in TMEM)
+                            mma_bf16(tmem + S_COL, sw128_desc(sKH + ks * 32, 0, 1024),
+                                     sw128_desc(sV + ks * 2048, BOX, 1024), ID_M128N128_KM, 1);
                         mma_commit(smem_u32(&aux.ds_full));
                         if (n + 1 < nch && !issue_ek(n + 1)) break;
                         if (!mbar_wait(smem_u32(&aux.ag_ready), n & 1, abort)) break;
@@ -430,29 +433,35 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         __syncwarp();
     } else if (rank == 0) {
         // ============================================================ CTA 0 element-wise
-        float Creg[64];  // C[c][64hf .. 64hf+64)
-        float m_cur;     // m[c] at the start of the current chunk
+        float m_cur;  // m[c] at the start of the current chunk
         bool fail = false;
         const float b_lam = p.lambda_in ? 0.f : p.b_lambda[h];
         uint8_t *dot = smem + CovLayout::DOT;
 
-        // ---- chunk 0 operands: C0 snapshot, m / w rows of the dot-product operand
+        // ---- C accumulator := C0; chunk 0 operands (C0 snapshot, m / w dot rows)
         {
-            const float *src = p.C0 ? p.C0 + ((size_t)bh * D + c) * D + 64 * hf : nullptr;
+            uint32_t cr[32];
+            const float *src = p.C0 ? p.C0 + ((size_t)bh * D + c) * D + 32 * qt : nullptr;
 #pragma unroll
-            for (int j = 0; j < 64; j += 4) {
+            for (int j = 0; j < 32; j += 4) {
                 const float4 v4 =
                     src ? *reinterpret_cast<const float4 *>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                Creg[j] = v4.x;
-                Creg[j + 1] = v4.y;
-                Creg[j + 2] = v4.z;
-                Creg[j + 3] = v4.w;
+                cr[j] = __float_as_uint(v4.x);
+                cr[j + 1] = __float_as_uint(v4.y);
+                cr[j + 2] = __float_as_uint(v4.z);
+                cr[j + 3] = __float_as_uint(v4.w);
             }
+            tmem_st32(tl + C_COL + 32 * qt, cr);
 #pragma unroll
-            for (int g = 0; g < 8; ++g)
-                store8_at(smem + CovLayout::C0 + sw128_chunk(c, 64 * hf + 8 * g, 128), Creg, 8 * g);
+            for (int g = 0; g < 4; ++g) {
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = u2f(cr[8 * g + e]);
+                store8(smem + CovLayout::C0 + sw128_chunk(c, 32 * qt + 8 * g, 128), v);
+            }
+            tmem_st_wait();
             m_cur = p.m0 ? p.m0[(size_t)bh * D + c] : 0.f;
-            if (hf == 0) {
+            if (qt == 0) {
                 const float w = p.lambda_in ? 0.f : p.w_lambda[(size_t)h * D + c];
                 const float mh = __bfloat162float(__float2bfloat16_rn(m_cur));
                 const float wh = __bfloat162float(__float2bfloat16_rn(w));
@@ -462,36 +471,40 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 put_bf16(dot + sw128_off(3, c, 16), w - wh);
             } else {
 #pragma unroll
-                for (int row = 4; row < 16; ++row) put_bf16(dot + sw128_off(row, c, 16), 0.f);
+                for (int row = 0; row < 4; ++row)
+                    put_bf16(dot + sw128_off(4 * qt + row, c, 16), 0.f);
             }
+            tc_fence_before();
             fence_async_smem();
             epi_sync_any(false);
             if (tid == 0) mbar_arrive(smem_u32(&aux.c0_ready));
         }
 
         for (int n = 0; n < nch; ++n) {
-            const int s = n & 1, b = n & 1;
+            const int b = n & 1;
             const uint32_t ph2 = (n >> 1) & 1;
             const int c0t = n * L;
             const int Lc = min(L, T - c0t);
             const bool more = n + 1 < nch;
             if (tid == 0) CCQ_TRACE(0, n, 0);
 
-            // ---- gate, s_i and Ah (rows in lanes 0-15; half hf takes 32 columns)
+            // ---- gate, s_i and Ah (rows in lanes 0-15; quarter qt takes 16 columns)
             bool ok = wait_all(smem_u32(&aux.aqk_full), n & 1, abort);
             tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 1);
-            uint32_t a[32], dt[4];
+            uint32_t a[16], dt[4];
             if (ok) {
-                tmem_ld32(tl + AQK_COL + 32 * hf, a);
+                tmem_ld16(tl + AQK_COL + 16 * qt, a);
                 tmem_ld4(tl + AQK_COL + 64, dt);
                 tmem_ld_wait();
                 if (tid == 0) CCQ_TRACE(0, n, 2);
-                float rs = 0.f;
+                float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (32 * hf + j <= r) rs += u2f(a[j]);
-                if (lane < 16) aux.part[hf][r] = rs;
+                for (int j = 0; j < 16; j += 2) {
+                    if (16 * qt + j <= r) rs0 += u2f(a[j]);
+                    if (16 * qt + j + 1 <= r) rs1 += u2f(a[j + 1]);
+                }
+                if (lane < 16) aux.part[qt][r] = rs0 + rs1;
             }
             if (epi_sync_any(!ok)) { fail = true; break; }
             if (tid == 0) CCQ_TRACE(0, n, 3);
@@ -499,26 +512,28 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 const bool valid = r < Lc;
                 const float mq = u2f(dt[0]) + u2f(dt[1]);
                 const float wq = u2f(dt[2]) + u2f(dt[3]);
-                const float rt = __frcp_rn((float)(p.t0 + (long long)(c0t + r + 1)));  // 1 / t_i
-                const float sdt = (mq + aux.part[0][r] + aux.part[1][r]) * rt;
-                if (hf == 0) {
+                const float rt = __fdividef(1.f, (float)(p.t0 + (long long)(c0t + r + 1)));  // 1/t_i
+                const float sdt =
+                    (mq + ((aux.part[0][r] + aux.part[1][r]) + (aux.part[2][r] + aux.part[3][r]))) * rt;
+                if (qt == 0) {
                     float lam = 0.f;
                     if (valid) {
                         const size_t ti = (size_t)bh * T + c0t + r;
-                        lam = p.lambda_in ? p.lambda_in[ti] : __frcp_rn(1.f + __expf(-(wq + b_lam)));
+                        lam = p.lambda_in ? p.lambda_in[ti]
+                                          : __fdividef(1.f, 1.f + __expf(-(wq + b_lam)));
                         if (p.lambda_out) p.lambda_out[ti] = lam;
                     }
                     aux.tok[r] = valid ? make_float2(lam * rt, sdt) : make_float2(0.f, 0.f);
                 }
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
+                for (int g = 0; g < 2; ++g) {
                     float v[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int j = 32 * hf + 8 * g + e;
+                        const int j = 16 * qt + 8 * g + e;
                         v[e] = (valid && j <= r) ? u2f(a[8 * g + e]) - sdt : 0.f;
                     }
-                    store8(smem + CovLayout::AH + sw128_chunk(r, 32 * hf + 8 * g, 64), v);
+                    store8(smem + CovLayout::AH + sw128_chunk(r, 16 * qt + 8 * g, 64), v);
                 }
             }
             tc_fence_before();
@@ -529,7 +544,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 CCQ_TRACE(0, n, 4);
             }
 
-            // ---- next chunk's operands: C += dC_n (registers), C0 snapshot, m += colsum K_n
+            // ---- next chunk's operands: C0 snapshot (C accumulator after dC_n), m += colsum K_n
             ok = wait_all(smem_u32(&aux.eq_full), n & 1, abort);
             if (more) ok = ok && wait_all(smem_u32(&aux.dc_full), n & 1, abort);
             tc_fence_after();
@@ -538,27 +553,25 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (ok) {
                 uint32_t ks[4];
                 tmem_ld4(tl + KS_COL, ks);
+                uint32_t cr[32];
+                if (more) tmem_ld32(tl + C_COL + 32 * qt, cr);
                 tmem_ld_wait();
-                m_next = m_cur + u2f(ks[0]);
                 if (tid == 0) CCQ_TRACE(0, n, 6);
-            }
-            if (ok && more) {
+                m_next = m_cur + u2f(ks[0]);
+                if (more) {
+                    uint8_t *c0n = smem + CovLayout::C0 + (b ^ 1) * 32768;
 #pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    uint32_t d[32];
-                    tmem_ld32(tl + DC_COL + 64 * hf + 32 * hb, d);
-                    tmem_ld_wait();
+                    for (int g = 0; g < 4; ++g) {
+                        float v[8];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) Creg[32 * hb + j] += u2f(d[j]);
-                }
-                uint8_t *c0n = smem + CovLayout::C0 + (b ^ 1) * 32768;
-#pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    store8_at(c0n + sw128_chunk(c, 64 * hf + 8 * g, 128), Creg, 8 * g);
-                if (hf == 0) {
-                    const float mh = __bfloat162float(__float2bfloat16_rn(m_next));
-                    put_bf16(dot + sw128_off(0, c, 16), mh);
-                    put_bf16(dot + sw128_off(1, c, 16), m_next - mh);
+                        for (int e = 0; e < 8; ++e) v[e] = u2f(cr[8 * g + e]);
+                        store8(c0n + sw128_chunk(c, 32 * qt + 8 * g, 128), v);
+                    }
+                    if (qt == 0) {
+                        const float mh = __bfloat162float(__float2bfloat16_rn(m_next));
+                        put_bf16(dot + sw128_off(0, c, 16), mh);
+                        put_bf16(dot + sw128_off(1, c, 16), m_next - mh);
+                    }
                 }
             }
             tc_fence_before();
@@ -570,34 +583,31 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 CCQ_TRACE(0, n, 7);
             }
 
-            // ---- cleaned, decay-scaled query Qt^T (thread = channel c, 32 tokens)
+            // ---- cleaned, decay-scaled query Qt^T (thread = channel c, 16 tokens)
             ok = wait_all(smem_u32(&aux.p_full[b]), ph2, abort);
             tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 8);
             if (ok) {
-                uint8_t *qt = smem + CovLayout::QT + b * 16384;
+                uint8_t *qtb = smem + CovLayout::QT + b * 16384;
+                const int i0 = 16 * qt;
+                uint32_t pr[16], er[16], qr[16];
+                tmem_ld16(tl + P_COL(b) + i0, pr);
+                tmem_ld16(tl + E0_COL + i0, er);
+                tmem_ld16(tl + QT_COL + i0, qr);
+                tmem_ld_wait();
+                if (tid == 0) CCQ_TRACE(0, n, 9);
+                if (qt == 0 && u2f(er[0]) < -80.f) record_status(p.status, CCQ_ERR_RANGE);
 #pragma unroll
-                for (int sb = 0; sb < 2; ++sb) {
-                    const int i0 = 32 * hf + 16 * sb;
-                    uint32_t pr[16], er[16], qr[16];
-                    tmem_ld16(tl + P_COL(b) + i0, pr);
-                    tmem_ld16(tl + E0_COL + i0, er);
-                    tmem_ld16(tl + QT_COL + i0, qr);
-                    tmem_ld_wait();
-                    if (tid == 0 && sb == 0) CCQ_TRACE(0, n, 9);
-                    if (i0 == 0 && u2f(er[0]) < -80.f) record_status(p.status, CCQ_ERR_RANGE);
+                for (int g = 0; g < 2; ++g) {
+                    float v[8];
 #pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        float v[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = 8 * g + e;
-                            const float2 tk = aux.tok[i0 + j];
-                            const float qc = u2f(qr[j]) - tk.x * (u2f(pr[j]) - tk.y * m_cur);
-                            v[e] = qc * exp2f(-1.4426950408889634f * u2f(er[j]));
-                        }
-                        store8(qt + sw128_chunk(c, i0 + 8 * g, 128), v);
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = 8 * g + e;
+                        const float2 tk = aux.tok[i0 + j];
+                        const float qc = u2f(qr[j]) - tk.x * (u2f(pr[j]) - tk.y * m_cur);
+                        v[e] = qc * exp2f(-1.4426950408889634f * u2f(er[j]));
                     }
+                    store8(qtb + sw128_chunk(c, i0 + 8 * g, 128), v);
                 }
             }
             tc_fence_before();
@@ -621,76 +631,53 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             }
             m_cur = m_next;
         }
-        // ---- final state: C = C + dC_last (registers), m
+        // ---- final state: C (TMEM accumulator), m
         if (!fail && nch > 0) {
             const bool ok = wait_all(smem_u32(&aux.dc_full), (nch - 1) & 1, abort);
             tc_fence_after();
             if (ok && p.C_out) {
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    uint32_t d[32];
-                    tmem_ld32(tl + DC_COL + 64 * hf + 32 * hb, d);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) Creg[32 * hb + j] += u2f(d[j]);
-                }
+                uint32_t cr[32];
+                tmem_ld32(tl + C_COL + 32 * qt, cr);
+                tmem_ld_wait();
                 float4 *dst =
-                    reinterpret_cast<float4 *>(p.C_out + ((size_t)bh * D + c) * D + 64 * hf);
+                    reinterpret_cast<float4 *>(p.C_out + ((size_t)bh * D + c) * D + 32 * qt);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    dst[j] = make_float4(Creg[4 * j], Creg[4 * j + 1], Creg[4 * j + 2], Creg[4 * j + 3]);
+                for (int j = 0; j < 8; ++j)
+                    dst[j] = make_float4(u2f(cr[4 * j]), u2f(cr[4 * j + 1]), u2f(cr[4 * j + 2]),
+                                         u2f(cr[4 * j + 3]));
             }
-            if (ok && p.m_out && hf == 0) p.m_out[(size_t)bh * D + c] = m_cur;
+            if (ok && p.m_out && qt == 0) p.m_out[(size_t)bh * D + c] = m_cur;
         }
         if (tid == 0) bulk_wait0();
     } else {
         // ============================================================ CTA 1 element-wise
-        float Sreg[64];  // S[c][64hf .. 64hf+64)
         bool fail = false;
-        {
-            const float *src = p.S0 ? p.S0 + ((size_t)bh * D + c) * D + 64 * hf : nullptr;
-#pragma unroll
-            for (int j = 0; j < 64; j += 4) {
-                const float4 v4 =
-                    src ? *reinterpret_cast<const float4 *>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-                Sreg[j] = v4.x;
-                Sreg[j + 1] = v4.y;
-                Sreg[j + 2] = v4.z;
-                Sreg[j + 3] = v4.w;
-            }
-        }
 
         // Kh^T = (K * exp(E))^T of chunk k from E^T, K^T in TMEM; gamma = exp(R)
         auto kh_phase = [&](int k, float &gam) -> bool {
             bool ok = wait_all(smem_u32(&aux.ek_full), k & 1, abort);
-            // Kh (single buffer) is still read by chunk k-1's dS product
+            // Kh (single buffer) is still read by chunk k-1's S update
             if (k > 0) ok = ok && wait_all(smem_u32(&aux.ds_full), (k - 1) & 1, abort);
             tc_fence_after();
             if (ok) {
-                uint8_t *kh = smem + GlaLayout::KH;
-#pragma unroll
-                for (int sb = 0; sb < 2; ++sb) {
-                    const int i0 = 32 * hf + 16 * sb;
-                    uint32_t er[16], kr[16];
-                    tmem_ld16(tl + E1_COL + i0, er);
-                    tmem_ld16(tl + KT_COL + i0, kr);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int g = 0; g < 2; ++g) {
-                        float v[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = 8 * g + e;
-                            v[e] = u2f(kr[j]) * exp2f(1.4426950408889634f * u2f(er[j]));
-                        }
-                        store8(kh + sw128_chunk(c, i0 + 8 * g, 128), v);
-                    }
-                }
-                uint32_t rr[4];
+                const int i0 = 16 * qt;
+                uint32_t er[16], kr[16], rr[4];
+                tmem_ld16(tl + E1_COL + i0, er);
+                tmem_ld16(tl + KT_COL + i0, kr);
                 tmem_ld4(tl + E1_COL + 64, rr);
                 tmem_ld_wait();
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = 8 * g + e;
+                        v[e] = u2f(kr[j]) * exp2f(1.4426950408889634f * u2f(er[j]));
+                    }
+                    store8(smem + GlaLayout::KH + sw128_chunk(c, i0 + 8 * g, 128), v);
+                }
                 const float R = u2f(rr[0]);
-                if (hf == 0 && R < -80.f) record_status(p.status, CCQ_ERR_RANGE);
+                if (qt == 0 && R < -80.f) record_status(p.status, CCQ_ERR_RANGE);
                 gam = exp2f(1.4426950408889634f * R);
             }
             tc_fence_before();
@@ -699,29 +686,41 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (tid == 0) mbar_arrive(smem_u32(&aux.kh_ready));
             return true;
         };
-        // Sb = gamma * (S + dS_{k-1}): the state operand of chunk k
+        // Sb = gamma * S: rescale the S accumulator in TMEM and snapshot it (bf16)
         auto sb_phase = [&](int k, float gam) -> bool {
             bool ok = true;
+            uint32_t sr[32];
             if (k > 0) {
                 ok = wait_all(smem_u32(&aux.ds_full), (k - 1) & 1, abort);
                 tc_fence_after();
                 if (ok) {
+                    tmem_ld32(tl + S_COL + 32 * qt, sr);
+                    tmem_ld_wait();
+                }
+            } else {
+                const float *src = p.S0 ? p.S0 + ((size_t)bh * D + c) * D + 32 * qt : nullptr;
 #pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        uint32_t d[32];
-                        tmem_ld32(tl + DS_COL + 64 * hf + 32 * hb, d);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) Sreg[32 * hb + j] += u2f(d[j]);
-                    }
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 v4 = src ? *reinterpret_cast<const float4 *>(src + j)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                    sr[j] = __float_as_uint(v4.x);
+                    sr[j + 1] = __float_as_uint(v4.y);
+                    sr[j + 2] = __float_as_uint(v4.z);
+                    sr[j + 3] = __float_as_uint(v4.w);
                 }
             }
             if (ok) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) Sreg[j] *= gam;
+                for (int j = 0; j < 32; ++j) sr[j] = __float_as_uint(gam * u2f(sr[j]));
+                tmem_st32(tl + S_COL + 32 * qt, sr);
 #pragma unroll
-                for (int g = 0; g < 8; ++g)
-                    store8_at(smem + GlaLayout::SB + sw128_chunk(c, 64 * hf + 8 * g, 128), Sreg, 8 * g);
+                for (int g = 0; g < 4; ++g) {
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = u2f(sr[8 * g + e]);
+                    store8(smem + GlaLayout::SB + sw128_chunk(c, 32 * qt + 8 * g, 128), v);
+                }
+                tmem_st_wait();
             }
             tc_fence_before();
             fence_async_smem();
@@ -740,22 +739,22 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             const int c0t = n * L;
             if (tid == 0) CCQ_TRACE(0, n, 0);
 
-            // ---- causal mask of Ag (rows in lanes 0-15; half hf takes 32 columns)
+            // ---- causal mask of Ag (rows in lanes 0-15; quarter qt takes 16 columns)
             bool ok = wait_all(smem_u32(&aux.stage1), n & 1, abort);
             tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 1);
             if (ok) {
-                uint32_t a[32];
-                tmem_ld32(tl + AG_COL + 32 * hf, a);
+                uint32_t a[16];
+                tmem_ld16(tl + AG_COL + 16 * qt, a);
                 tmem_ld_wait();
                 if (lane < 16) {
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
+                    for (int g = 0; g < 2; ++g) {
                         float v[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
-                            v[e] = (32 * hf + 8 * g + e <= r) ? u2f(a[8 * g + e]) : 0.f;
-                        store8(smem + GlaLayout::AG + sw128_chunk(r, 32 * hf + 8 * g, 64), v);
+                            v[e] = (16 * qt + 8 * g + e <= r) ? u2f(a[8 * g + e]) : 0.f;
+                        store8(smem + GlaLayout::AG + sw128_chunk(r, 16 * qt + 8 * g, 64), v);
                     }
                 }
             }
@@ -780,15 +779,11 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (tid == 0) CCQ_TRACE(0, n, 4);
             if (ok) {
                 uint8_t *sO = smem + GlaLayout::O;
+                uint32_t o[16];
+                tmem_ld16(tl + O_COL(b) + 16 * qt, o);
+                tmem_ld_wait();
 #pragma unroll
-                for (int sb = 0; sb < 2; ++sb) {
-                    uint32_t o[16];
-                    tmem_ld16(tl + O_COL(b) + 32 * hf + 16 * sb, o);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        put_bf16(sO + sw128_off(32 * hf + 16 * sb + j, c, 64), u2f(o[j]));
-                }
+                for (int j = 0; j < 16; ++j) put_bf16(sO + sw128_off(16 * qt + j, c, 64), u2f(o[j]));
             }
             tc_fence_before();
             fence_async_smem();
@@ -804,24 +799,20 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             // ---- next chunk's Sb snapshot
             if (n + 1 < nch && !sb_phase(n + 1, gam_next)) { fail = true; break; }
         }
-        // ---- final state S = Sb_last + dS_last
+        // ---- final state S (TMEM accumulator)
         if (!fail && nch > 0 && p.S_out) {
             const bool ok = wait_all(smem_u32(&aux.ds_full), (nch - 1) & 1, abort);
             tc_fence_after();
             if (ok) {
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb) {
-                    uint32_t d[32];
-                    tmem_ld32(tl + DS_COL + 64 * hf + 32 * hb, d);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) Sreg[32 * hb + j] += u2f(d[j]);
-                }
+                uint32_t sr[32];
+                tmem_ld32(tl + S_COL + 32 * qt, sr);
+                tmem_ld_wait();
                 float4 *dst =
-                    reinterpret_cast<float4 *>(p.S_out + ((size_t)bh * D + c) * D + 64 * hf);
+                    reinterpret_cast<float4 *>(p.S_out + ((size_t)bh * D + c) * D + 32 * qt);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    dst[j] = make_float4(Sreg[4 * j], Sreg[4 * j + 1], Sreg[4 * j + 2], Sreg[4 * j + 3]);
+                for (int j = 0; j < 8; ++j)
+                    dst[j] = make_float4(u2f(sr[4 * j]), u2f(sr[4 * j + 1]), u2f(sr[4 * j + 2]),
+                                         u2f(sr[4 * j + 3]));
             }
         }
         if (tid == 0) bulk_wait0();
