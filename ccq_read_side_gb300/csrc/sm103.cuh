@@ -82,9 +82,10 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int *abort, bool cluster_scope = false) {
-    if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+// Slow path of a bounded wait, kept out of line so the many wait sites stay
+// small (the kernels' hot loops must fit the instruction cache).
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
+                                            bool cluster_scope) {
     const unsigned long long t0 = globaltimer_ns();
     for (unsigned it = 1;; ++it) {
         if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
@@ -96,6 +97,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
             }
         }
     }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int *abort, bool cluster_scope = false) {
+    if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, abort, cluster_scope);
 }
 
 __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {

@@ -193,12 +193,36 @@ constexpr uint32_t ID_M128N128_KM = idesc_bf16(128, 128, 0, 1);
 constexpr uint32_t ID_M128N80_MK = idesc_bf16(128, 80, 1, 0);
 constexpr uint32_t ID_M128N16_MK = idesc_bf16(128, 16, 1, 0);
 
+
+// Issues nk MMAs (K = 16 each) into d; the k-th uses operand byte offsets
+// koff(k) on both descriptors' start addresses.  Rolled on purpose: the hot
+// loops of this kernel must fit the instruction cache.
+//   K-major operand, 64-wide K blocks `blk` bytes apart: koff = (k/4)*blk + (k%4)*32
+//   MN-major operand (rows are K): koff = k * 2048
+__device__ __forceinline__ uint32_t koff_k(int k, uint32_t blk) { return (k >> 2) * blk + (k & 3) * 32; }
+__device__ __forceinline__ uint32_t koff_mn(int k) { return (uint32_t)k * 2048u; }
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+template <bool A_MN, bool B_MN>
+__device__ __noinline__ void mma_k_loop(uint32_t d, uint64_t adesc, uint32_t ablk, uint64_t bdesc,
+                                        uint32_t bblk, uint32_t idesc, int nk, uint32_t acc0) {
+#pragma unroll 1
+    for (int k = 0; k < nk; ++k) {
+        const uint32_t ao = A_MN ? koff_mn(k) : koff_k(k, ablk);
+        const uint32_t bo = B_MN ? koff_mn(k) : koff_k(k, bblk);
+        mma_bf16(d, desc_add(adesc, ao), desc_add(bdesc, bo), idesc, (k > 0) | acc0);
+    }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
 tc_gla_kernel(const __grid_constant__ Args args) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     Aux &aux = *reinterpret_cast<Aux *>(smem + TILES_END);
-    const CcqParams &p = args.p;
+    // Copy the scalar arguments out of parameter space once (a reference into
+    // a __grid_constant__ parameter is a generic pointer: every field access
+    // would be a long-latency load).
+    const CcqParams p = args.p;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
@@ -308,60 +332,45 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     if (!mbar_wait(smem_u32(&aux.full[s]), ph2, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 0);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks) {  // A = Q K^T
-                        const uint32_t off = (ks >> 2) * BOX + (ks & 3) * 32;
-                        mma_bf16(tmem + AQK_COL, sw128_desc(sQ + off, 0, 1024),
-                                 sw128_desc(sK + off, 0, 1024), ID_M64N64_KK, ks > 0);
-                    }
+                    // A = Q K^T
+                    mma_k_loop<false, false>(tmem + AQK_COL, sw128_desc(sQ, 0, 1024), BOX,
+                                             sw128_desc(sK, 0, 1024), BOX, ID_M64N64_KK, 8, 0);
                     CCQ_TRACE(1, n, 4);
                     if (!mbar_wait(smem_u32(&aux.c0_ready), n & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 1);
                     const uint32_t sDOT = smem_u32(smem + CovLayout::DOT);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)  // [m_hi m_lo w_hi w_lo] . q
-                        mma_bf16(tmem + AQK_COL + 64,
-                                 sw128_desc(sQ + (ks >> 2) * BOX + (ks & 3) * 32, 0, 1024),
-                                 sw128_desc(sDOT + (ks >> 2) * 2048 + (ks & 3) * 32, 0, 1024),
-                                 ID_M64N16_KK, ks > 0);
+                    // [m_hi m_lo w_hi w_lo] . q
+                    mma_k_loop<false, false>(tmem + AQK_COL + 64, sw128_desc(sQ, 0, 1024), BOX,
+                                             sw128_desc(sDOT, 0, 1024), 2048, ID_M64N16_KK, 8, 0);
                     mma_commit(smem_u32(&aux.aqk_full));
                     const uint32_t sC0 = smem_u32(smem + CovLayout::C0 + b * 32768);
-#pragma unroll
-                    for (int ks = 0; ks < 8; ++ks)  // P^T = C0 Q^T
-                        mma_bf16(tmem + P_COL(b),
-                                 sw128_desc(sC0 + (ks >> 2) * 16384 + (ks & 3) * 32, 0, 1024),
-                                 sw128_desc(sQ + (ks >> 2) * BOX + (ks & 3) * 32, 0, 1024),
-                                 ID_M128N64_KK, ks > 0);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {  // C += K^T K
-                        const uint64_t dk = sw128_desc(sK + ks * 2048, BOX, 1024);
-                        mma_bf16(tmem + C_COL, dk, dk, ID_M128N128_MM, 1);
-                    }
+                    // P^T = C0 Q^T
+                    mma_k_loop<false, false>(tmem + P_COL(b), sw128_desc(sC0, 0, 1024), 16384,
+                                             sw128_desc(sQ, 0, 1024), BOX, ID_M128N64_KK, 8, 0);
+                    // C += K^T K
+                    mma_k_loop<true, true>(tmem + C_COL, sw128_desc(sK, BOX, 1024), 0,
+                                           sw128_desc(sK, BOX, 1024), 0, ID_M128N128_MM, 4, 1);
                     mma_commit(smem_u32(&aux.dc_full));
                     if (n > 0 && !mbar_wait(smem_u32(&aux.eq_free), (n - 1) & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 5);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {  // E^T = LA^T U^T, Q^T, colsum(K)
-                        const uint64_t ub = sw128_desc(sUX + ks * 32, 0, 1024);
-                        mma_bf16(tmem + E0_COL, sw128_desc(sLA + ks * 2048, BOX, 1024), ub,
-                                 ID_M128N64_MK, ks > 0);
-                        mma_bf16(tmem + QT_COL, sw128_desc(sQ + ks * 2048, BOX, 1024),
-                                 sw128_desc(sID + ks * 32, 0, 1024), ID_M128N64_MK, ks > 0);
-                        mma_bf16(tmem + KS_COL, sw128_desc(sK + ks * 2048, BOX, 1024),
-                                 sw128_desc(sUX + 64 * 128 + ks * 32, 0, 1024), ID_M128N16_MK,
-                                 ks > 0);
-                    }
+                    // E^T = LA^T U^T, Q^T, colsum(K)
+                    mma_k_loop<true, false>(tmem + E0_COL, sw128_desc(sLA, BOX, 1024), 0,
+                                            sw128_desc(sUX, 0, 1024), 0, ID_M128N64_MK, 4, 0);
+                    mma_k_loop<true, false>(tmem + QT_COL, sw128_desc(sQ, BOX, 1024), 0,
+                                            sw128_desc(sID, 0, 1024), 0, ID_M128N64_MK, 4, 0);
+                    mma_k_loop<true, false>(tmem + KS_COL, sw128_desc(sK, BOX, 1024), 0,
+                                            sw128_desc(sUX + 64 * 128, 0, 1024), 0, ID_M128N16_MK,
+                                            4, 0);
                     mma_commit(smem_u32(&aux.eq_full));
                     if (!mbar_wait(smem_u32(&aux.ahat_ready), n & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 2);
                     const uint32_t sAH = smem_u32(smem + CovLayout::AH);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks)  // P^T += K^T Ah^T
-                        mma_bf16(tmem + P_COL(b), sw128_desc(sK + ks * 2048, BOX, 1024),
-                                 sw128_desc(sAH + ks * 32, 0, 1024), ID_M128N64_MK, 1);
+                    // P^T += K^T Ah^T
+                    mma_k_loop<true, false>(tmem + P_COL(b), sw128_desc(sK, BOX, 1024), 0,
+                                            sw128_desc(sAH, 0, 1024), 0, ID_M128N64_MK, 4, 1);
                     mma_commit(smem_u32(&aux.p_full[b]));
                     mma_commit(smem_u32(&aux.empty[s]));
                     CCQ_TRACE(1, n, 3);
@@ -374,13 +383,10 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     tc_fence_after();
                     const uint32_t sK = smem_u32(smem + GlaLayout::K + s * TILE);
                     const uint32_t sLA = smem_u32(smem + GlaLayout::LA + s * TILE);
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        mma_bf16(tmem + E1_COL, sw128_desc(sLA + ks * 2048, BOX, 1024),
-                                 sw128_desc(sUX + ks * 32, 0, 1024), ID_M128N80_MK, ks > 0);
-                        mma_bf16(tmem + KT_COL, sw128_desc(sK + ks * 2048, BOX, 1024),
-                                 sw128_desc(sID + ks * 32, 0, 1024), ID_M128N64_MK, ks > 0);
-                    }
+                    mma_k_loop<true, false>(tmem + E1_COL, sw128_desc(sLA, BOX, 1024), 0,
+                                            sw128_desc(sUX, 0, 1024), 0, ID_M128N80_MK, 4, 0);
+                    mma_k_loop<true, false>(tmem + KT_COL, sw128_desc(sK, BOX, 1024), 0,
+                                            sw128_desc(sID, 0, 1024), 0, ID_M128N64_MK, 4, 0);
                     mma_commit(smem_u32(&aux.ek_full));
                     return true;
                 };
@@ -399,30 +405,24 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                         if (!mbar_wait(smem_u32(&aux.qt_full[b]), ph2, abort, true)) break;
                         tc_fence_after();
                         CCQ_TRACE(1, n, 1);
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks)  // Ag = Qt Kh^T (channel-major operands)
-                            mma_bf16(tmem + AG_COL, sw128_desc(sQT + ks * 2048, 16384, 1024),
-                                     sw128_desc(sKH + ks * 2048, 16384, 1024), ID_M64N64_MM,
-                                     ks > 0);
-#pragma unroll
-                        for (int ks = 0; ks < 8; ++ks)  // O^T = Sb^T Qt^T
-                            mma_bf16(tmem + O_COL(b), sw128_desc(sSB + ks * 2048, 16384, 1024),
-                                     sw128_desc(sQT + ks * 2048, 16384, 1024), ID_M128N64_MM,
-                                     ks > 0);
+                        // Ag = Qt Kh^T (channel-major operands)
+                        mma_k_loop<true, true>(tmem + AG_COL, sw128_desc(sQT, 16384, 1024), 0,
+                                               sw128_desc(sKH, 16384, 1024), 0, ID_M64N64_MM, 8, 0);
+                        // O^T = Sb^T Qt^T
+                        mma_k_loop<true, true>(tmem + O_COL(b), sw128_desc(sSB, 16384, 1024), 0,
+                                               sw128_desc(sQT, 16384, 1024), 0, ID_M128N64_MM, 8, 0);
                         mma_commit(smem_u32(&aux.stage1));
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)  // S = Sb + Kh^T V (Sb already in TMEM)
-                            mma_bf16(tmem + S_COL, sw128_desc(sKH + ks * 32, 0, 1024),
-                                     sw128_desc(sV + ks * 2048, BOX, 1024), ID_M128N128_KM, 1);
+                        // S = Sb + Kh^T V (Sb already in TMEM)
+                        mma_k_loop<false, true>(tmem + S_COL, sw128_desc(sKH, 0, 1024), 0,
+                                                sw128_desc(sV, BOX, 1024), 0, ID_M128N128_KM, 4, 1);
                         mma_commit(smem_u32(&aux.ds_full));
                         if (n + 1 < nch && !issue_ek(n + 1)) break;
                         if (!mbar_wait(smem_u32(&aux.ag_ready), n & 1, abort)) break;
                         tc_fence_after();
                         CCQ_TRACE(1, n, 2);
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)  // O^T += V^T Ag^T
-                            mma_bf16(tmem + O_COL(b), sw128_desc(sV + ks * 2048, BOX, 1024),
-                                     sw128_desc(sAG + ks * 32, 0, 1024), ID_M128N64_MK, 1);
+                        // O^T += V^T Ag^T
+                        mma_k_loop<true, false>(tmem + O_COL(b), sw128_desc(sV, BOX, 1024), 0,
+                                                sw128_desc(sAG, 0, 1024), 0, ID_M128N64_MK, 4, 1);
                         mma_commit(smem_u32(&aux.o_full[b]));
                         mma_commit(smem_u32(&aux.empty[s]));
                         CCQ_TRACE(1, n, 3);
