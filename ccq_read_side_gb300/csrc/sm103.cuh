@@ -82,14 +82,16 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
     return t;
 }
 
-// Slow path of a bounded wait, kept out of line so the many wait sites stay
-// small (the kernels' hot loops must fit the instruction cache).
-__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int *abort,
-                                            bool cluster_scope) {
+// Bounded wait: one fast try_wait; the polling loop is kept compact (a
+// wall-clock check every 64 polls) so the many wait sites stay small.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          volatile int *abort, bool cluster_scope = false) {
+    if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
     const unsigned long long t0 = globaltimer_ns();
+#pragma unroll 1
     for (unsigned it = 1;; ++it) {
         if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
-        if ((it & 15u) == 0) {
+        if ((it & 63u) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > kWaitNs) {
                 *abort = 1;
@@ -97,12 +99,6 @@ __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volat
             }
         }
     }
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int *abort, bool cluster_scope = false) {
-    if (cluster_scope ? mbar_test_cluster(bar, parity) : mbar_test(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, abort, cluster_scope);
 }
 
 __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
@@ -252,6 +248,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"

@@ -204,7 +204,7 @@ __device__ __forceinline__ uint32_t koff_mn(int k) { return (uint32_t)k * 2048u;
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 template <bool A_MN, bool B_MN>
-__device__ __noinline__ void mma_k_loop(uint32_t d, uint64_t adesc, uint32_t ablk, uint64_t bdesc,
+__device__ __forceinline__ void mma_k_loop(uint32_t d, uint64_t adesc, uint32_t ablk, uint64_t bdesc,
                                         uint32_t bblk, uint32_t idesc, int nk, uint32_t acc0) {
 #pragma unroll 1
     for (int k = 0; k < nk; ++k) {
@@ -553,19 +553,23 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (ok) {
                 uint32_t ks[4];
                 tmem_ld4(tl + KS_COL, ks);
-                uint32_t cr[32];
-                if (more) tmem_ld32(tl + C_COL + 32 * qt, cr);
                 tmem_ld_wait();
                 if (tid == 0) CCQ_TRACE(0, n, 6);
                 m_next = m_cur + u2f(ks[0]);
                 if (more) {
                     uint8_t *c0n = smem + CovLayout::C0 + (b ^ 1) * 32768;
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        float v[8];
+                    for (int hb = 0; hb < 2; ++hb) {
+                        uint32_t cr[16];
+                        tmem_ld16(tl + C_COL + 32 * qt + 16 * hb, cr);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = u2f(cr[8 * g + e]);
-                        store8(c0n + sw128_chunk(c, 32 * qt + 8 * g, 128), v);
+                        for (int g = 0; g < 2; ++g) {
+                            float v[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = u2f(cr[8 * g + e]);
+                            store8(c0n + sw128_chunk(c, 32 * qt + 16 * hb + 8 * g, 128), v);
+                        }
                     }
                     if (qt == 0) {
                         const float mh = __bfloat162float(__float2bfloat16_rn(m_next));
@@ -589,25 +593,24 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (tid == 0) CCQ_TRACE(0, n, 8);
             if (ok) {
                 uint8_t *qtb = smem + CovLayout::QT + b * 16384;
-                const int i0 = 16 * qt;
-                uint32_t pr[16], er[16], qr[16];
-                tmem_ld16(tl + P_COL(b) + i0, pr);
-                tmem_ld16(tl + E0_COL + i0, er);
-                tmem_ld16(tl + QT_COL + i0, qr);
-                tmem_ld_wait();
-                if (tid == 0) CCQ_TRACE(0, n, 9);
-                if (qt == 0 && u2f(er[0]) < -80.f) record_status(p.status, CCQ_ERR_RANGE);
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
+                    const int i0 = 16 * qt + 8 * g;
+                    uint32_t pr[8], er[8], qr[8];
+                    tmem_ld8(tl + P_COL(b) + i0, pr);
+                    tmem_ld8(tl + E0_COL + i0, er);
+                    tmem_ld8(tl + QT_COL + i0, qr);
+                    tmem_ld_wait();
+                    if (tid == 0 && g == 0) CCQ_TRACE(0, n, 9);
+                    if (i0 == 0 && u2f(er[0]) < -80.f) record_status(p.status, CCQ_ERR_RANGE);
                     float v[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int j = 8 * g + e;
-                        const float2 tk = aux.tok[i0 + j];
-                        const float qc = u2f(qr[j]) - tk.x * (u2f(pr[j]) - tk.y * m_cur);
-                        v[e] = qc * exp2f(-1.4426950408889634f * u2f(er[j]));
+                        const float2 tk = aux.tok[i0 + e];
+                        const float qc = u2f(qr[e]) - tk.x * (u2f(pr[e]) - tk.y * m_cur);
+                        v[e] = qc * exp2f(-1.4426950408889634f * u2f(er[e]));
                     }
-                    store8(qtb + sw128_chunk(c, i0 + 8 * g, 128), v);
+                    store8(qtb + sw128_chunk(c, i0, 128), v);
                 }
             }
             tc_fence_before();
