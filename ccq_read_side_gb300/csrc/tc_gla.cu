@@ -65,17 +65,17 @@ constexpr uint32_t BOX = L * 64 * 2;  // 8 KB
 // use the 128-byte swizzle (sw128_off / sw128_chunk).  The three input tiles
 // of a stage sit at the same offsets in both CTAs (CTA 0: Q, K, log alpha;
 // CTA 1: K, log alpha, V).
+constexpr uint32_t KBLK = 10240;       // CTA 0 K tile: 64-column block = 64 K rows + 16 dot rows
+constexpr uint32_t KTILE = 2 * KBLK;
 struct CovLayout {  // CTA 0
-    static constexpr uint32_t Q = 0;               // 2 stages x [64 tok][128]
-    static constexpr uint32_t K = Q + 2 * TILE;
-    static constexpr uint32_t LA = K + 2 * TILE;   // log alpha
-    static constexpr uint32_t C0 = LA + 2 * TILE;  // 2 x bf16 C0 snapshot, K-major [128][128]
-    static constexpr uint32_t AH = C0 + 65536;     // bf16 Ah [64 q][64 k]
-    static constexpr uint32_t DOT = AH + 8192;     // bf16 [16 rows][128]: m_hi m_lo w_hi w_lo 0..
-    static constexpr uint32_t QT = DOT + 4096;     // 2 x bf16 Qt^T [128 ch][64 tok] (send)
-    static constexpr uint32_t UX = QT + 32768;     // constant U operand (see below)
-    static constexpr uint32_t ID = UX + 10240;     // constant 64x64 identity
-    static constexpr uint32_t END = ID + 8192;
+    static constexpr uint32_t Q = 0;                // 2 stages x [64 tok][128]
+    static constexpr uint32_t K = Q + 2 * TILE;     // 2 stages x 2 blocks x [80 rows][64]
+    static constexpr uint32_t LA = K + 2 * KTILE;   // log alpha
+    static constexpr uint32_t C0 = LA + 2 * TILE;   // 2 x bf16 C0 snapshot, K-major [128][128]
+    static constexpr uint32_t AH = C0 + 65536;      // bf16 Ah [64 q][64 k]
+    static constexpr uint32_t QT = AH + 8192;       // 2 x bf16 Qt^T [128 ch][64 tok] (send)
+    static constexpr uint32_t UX = QT + 32768;      // constant U operand (see below)
+    static constexpr uint32_t END = UX + 10240;
 };
 struct GlaLayout {  // CTA 1
     static constexpr uint32_t K = 0;               // 2 stages
@@ -87,14 +87,20 @@ struct GlaLayout {  // CTA 1
     static constexpr uint32_t QTR = AG + 8192;     // 2 x Qt^T receive slots
     static constexpr uint32_t O = QTR + 32768;     // bf16 O tile [64 tok][128]
     static constexpr uint32_t UX = O + 16384;
-    static constexpr uint32_t ID = UX + 10240;
-    static constexpr uint32_t END = ID + 8192;
+    static constexpr uint32_t END = UX + 10240;
 };
 constexpr uint32_t TILES_END = GlaLayout::END > CovLayout::END ? GlaLayout::END : CovLayout::END;
+// CTA 0's K tile stores, after the 64 token rows of each 64-channel block,
+// 16 "dot" rows: m_hi, m_lo, w_hi, w_lo, then zeros.  One M=64, N=80 MMA of
+// Q against it yields Q K^T and the four dot products m.q and w.q at once.
+__host__ __device__ constexpr uint32_t dot_off(int s, int row, int c) {
+    return CovLayout::K + s * KTILE + (c >> 6) * KBLK + 8192 + row * 128 +
+           ((((c & 63) >> 3) ^ (row & 7)) << 4) + ((c & 7) << 1);
+}
 // UX: K-major B operand [80 rows][64 tokens]: row i < 64 holds ones at token
 // columns i' > i (the strictly-upper ones matrix, so LA^T U^T gives the
 // exclusive suffix sums), row 64 is all ones (chunk totals / column sums),
-// rows 65-79 are zero.  ID: the 64x64 identity (Q^T, K^T into TMEM).
+// rows 65-79 are zero.
 
 struct Aux {
     uint64_t full[2], empty[2];                                                 // TMA stages
@@ -114,13 +120,11 @@ constexpr uint32_t C_COL = 0;      // CTA 0: C accumulator (128)
 constexpr uint32_t AQK_COL = 128;  //        A (64) + dots (16)
 __host__ __device__ constexpr uint32_t P_COL(int b) { return 224 + 64 * b; }
 constexpr uint32_t E0_COL = 352;   //        E^T (64)
-constexpr uint32_t QT_COL = 416;   //        Q^T (64)
 constexpr uint32_t KS_COL = 480;   //        colsum(K) (16)
 constexpr uint32_t S_COL = 0;      // CTA 1: S accumulator (128)
 constexpr uint32_t AG_COL = 128;   //        Ag (64)
 __host__ __device__ constexpr uint32_t O_COL(int b) { return 192 + 64 * b; }
 constexpr uint32_t E1_COL = 320;   //        E^T (64) + R (16)
-constexpr uint32_t KT_COL = 400;   //        K^T (64)
 constexpr uint32_t TMEM_COLS = 512;
 
 struct Args {
@@ -183,7 +187,7 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile
 
 // Instruction descriptors (bf16 x bf16 -> fp32); K = K-major, M = MN-major.
 constexpr uint32_t ID_M64N64_KK = idesc_bf16(64, 64, 0, 0);
-constexpr uint32_t ID_M64N16_KK = idesc_bf16(64, 16, 0, 0);
+constexpr uint32_t ID_M64N80_KK = idesc_bf16(64, 80, 0, 0);
 constexpr uint32_t ID_M64N64_MM = idesc_bf16(64, 64, 1, 1);
 constexpr uint32_t ID_M128N64_KK = idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t ID_M128N64_MK = idesc_bf16(128, 64, 1, 0);
@@ -231,7 +235,6 @@ tc_gla_kernel(const __grid_constant__ Args args) {
     const int nch = (T + L - 1) / L;
     volatile int *abort = &aux.abort;
     const uint32_t UXo = rank == 0 ? CovLayout::UX : GlaLayout::UX;
-    const uint32_t IDo = rank == 0 ? CovLayout::ID : GlaLayout::ID;
 
     // ------------------------------------------------------------ set-up
     if (tid == 0) {
@@ -258,15 +261,11 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         mbar_init(smem_u32(&aux.ag_ready), 1);
         fence_mbar_init();
     }
-    if (warp < NEPI / 32) {  // constant operands U (with the ones row) and the identity
+    if (warp < NEPI / 32) {  // constant operand U (with the ones row)
         for (int x = tid; x < 80 * 64; x += NEPI) {
             const int row = x >> 6, col = x & 63;
             const float v = row < 64 ? (col > row ? 1.f : 0.f) : (row == 64 ? 1.f : 0.f);
             put_bf16(smem + UXo + sw128_off(row, col, 80), v);
-        }
-        for (int x = tid; x < 64 * 64; x += NEPI) {
-            const int row = x >> 6, col = x & 63;
-            put_bf16(smem + IDo + sw128_off(row, col, 64), row == col ? 1.f : 0.f);
         }
         fence_async_smem();
     }
@@ -298,6 +297,10 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             const CUtensorMap *m0 = rank == 0 ? &args.mq : &args.mk;
             const CUtensorMap *m1 = rank == 0 ? &args.mk : &args.mla;
             const CUtensorMap *m2 = rank == 0 ? &args.mla : &args.mv;
+            // CTA 0: Q, K (80-row blocks), log alpha; CTA 1: K, log alpha, V
+            const uint32_t base1 = rank == 0 ? CovLayout::K : GlaLayout::LA;
+            const uint32_t base2 = rank == 0 ? CovLayout::LA : GlaLayout::V;
+            const uint32_t stage1 = rank == 0 ? KTILE : TILE, blk1 = rank == 0 ? KBLK : BOX;
             for (int n = 0; n < nch; ++n) {
                 const int s = n & 1;
                 if (n >= 2 && !mbar_wait(smem_u32(&aux.empty[s]), ((n >> 1) - 1) & 1, abort))
@@ -306,13 +309,11 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 const uint32_t fb = smem_u32(&aux.full[s]);
                 mbar_expect_tx(fb, 3 * TILE);
                 for (int b = 0; b < 2; ++b) {
-                    // CTA 0: Q, K, log alpha; CTA 1: K, log alpha, V (same stage offsets)
-                    tma_load_3d(smem_u32(smem + 0 * TILE * 2 + s * TILE + b * BOX), m0, fb,
-                                b * 64, n * L, bh);
-                    tma_load_3d(smem_u32(smem + 1 * TILE * 2 + s * TILE + b * BOX), m1, fb,
-                                b * 64, n * L, bh);
-                    tma_load_3d(smem_u32(smem + 2 * TILE * 2 + s * TILE + b * BOX), m2, fb,
-                                b * 64, n * L, bh);
+                    tma_load_3d(smem_u32(smem + s * TILE + b * BOX), m0, fb, b * 64, n * L, bh);
+                    tma_load_3d(smem_u32(smem + base1 + s * stage1 + b * blk1), m1, fb, b * 64,
+                                n * L, bh);
+                    tma_load_3d(smem_u32(smem + base2 + s * TILE + b * BOX), m2, fb, b * 64,
+                                n * L, bh);
                 }
             }
         }
@@ -321,46 +322,39 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         // ============================================================ MMA issuer
         if (lane == 0) {
             const uint32_t sUX = smem_u32(smem + UXo);
-            const uint32_t sID = smem_u32(smem + IDo);
             if (rank == 0) {
                 for (int n = 0; n < nch; ++n) {
                     const int s = n & 1, b = n & 1;
                     const uint32_t ph2 = (n >> 1) & 1;
                     const uint32_t sQ = smem_u32(smem + CovLayout::Q + s * TILE);
-                    const uint32_t sK = smem_u32(smem + CovLayout::K + s * TILE);
+                    const uint32_t sK = smem_u32(smem + CovLayout::K + s * KTILE);
                     const uint32_t sLA = smem_u32(smem + CovLayout::LA + s * TILE);
                     if (!mbar_wait(smem_u32(&aux.full[s]), ph2, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 0);
-                    // A = Q K^T
-                    mma_k_loop<false, false>(tmem + AQK_COL, sw128_desc(sQ, 0, 1024), BOX,
-                                             sw128_desc(sK, 0, 1024), BOX, ID_M64N64_KK, 8, 0);
                     CCQ_TRACE(1, n, 4);
                     if (!mbar_wait(smem_u32(&aux.c0_ready), n & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 1);
-                    const uint32_t sDOT = smem_u32(smem + CovLayout::DOT);
-                    // [m_hi m_lo w_hi w_lo] . q
-                    mma_k_loop<false, false>(tmem + AQK_COL + 64, sw128_desc(sQ, 0, 1024), BOX,
-                                             sw128_desc(sDOT, 0, 1024), 2048, ID_M64N16_KK, 8, 0);
+                    // [A | m_hi.q m_lo.q w_hi.q w_lo.q] = Q [K | dot rows]^T
+                    mma_k_loop<false, false>(tmem + AQK_COL, sw128_desc(sQ, 0, 1024), BOX,
+                                             sw128_desc(sK, 0, 1024), KBLK, ID_M64N80_KK, 8, 0);
                     mma_commit(smem_u32(&aux.aqk_full));
                     const uint32_t sC0 = smem_u32(smem + CovLayout::C0 + b * 32768);
                     // P^T = C0 Q^T
                     mma_k_loop<false, false>(tmem + P_COL(b), sw128_desc(sC0, 0, 1024), 16384,
                                              sw128_desc(sQ, 0, 1024), BOX, ID_M128N64_KK, 8, 0);
                     // C += K^T K
-                    mma_k_loop<true, true>(tmem + C_COL, sw128_desc(sK, BOX, 1024), 0,
-                                           sw128_desc(sK, BOX, 1024), 0, ID_M128N128_MM, 4, 1);
+                    mma_k_loop<true, true>(tmem + C_COL, sw128_desc(sK, KBLK, 1024), 0,
+                                           sw128_desc(sK, KBLK, 1024), 0, ID_M128N128_MM, 4, 1);
                     mma_commit(smem_u32(&aux.dc_full));
                     if (n > 0 && !mbar_wait(smem_u32(&aux.eq_free), (n - 1) & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 5);
-                    // E^T = LA^T U^T, Q^T, colsum(K)
+                    // E^T = LA^T U^T, colsum(K)
                     mma_k_loop<true, false>(tmem + E0_COL, sw128_desc(sLA, BOX, 1024), 0,
                                             sw128_desc(sUX, 0, 1024), 0, ID_M128N64_MK, 4, 0);
-                    mma_k_loop<true, false>(tmem + QT_COL, sw128_desc(sQ, BOX, 1024), 0,
-                                            sw128_desc(sID, 0, 1024), 0, ID_M128N64_MK, 4, 0);
-                    mma_k_loop<true, false>(tmem + KS_COL, sw128_desc(sK, BOX, 1024), 0,
+                    mma_k_loop<true, false>(tmem + KS_COL, sw128_desc(sK, KBLK, 1024), 0,
                                             sw128_desc(sUX + 64 * 128, 0, 1024), 0, ID_M128N16_MK,
                                             4, 0);
                     mma_commit(smem_u32(&aux.eq_full));
@@ -369,7 +363,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     CCQ_TRACE(1, n, 2);
                     const uint32_t sAH = smem_u32(smem + CovLayout::AH);
                     // P^T += K^T Ah^T
-                    mma_k_loop<true, false>(tmem + P_COL(b), sw128_desc(sK, BOX, 1024), 0,
+                    mma_k_loop<true, false>(tmem + P_COL(b), sw128_desc(sK, KBLK, 1024), 0,
                                             sw128_desc(sAH, 0, 1024), 0, ID_M128N64_MK, 4, 1);
                     mma_commit(smem_u32(&aux.p_full[b]));
                     mma_commit(smem_u32(&aux.empty[s]));
@@ -381,12 +375,9 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     const int s = k & 1;
                     if (!mbar_wait(smem_u32(&aux.full[s]), (k >> 1) & 1, abort)) return false;
                     tc_fence_after();
-                    const uint32_t sK = smem_u32(smem + GlaLayout::K + s * TILE);
                     const uint32_t sLA = smem_u32(smem + GlaLayout::LA + s * TILE);
                     mma_k_loop<true, false>(tmem + E1_COL, sw128_desc(sLA, BOX, 1024), 0,
                                             sw128_desc(sUX, 0, 1024), 0, ID_M128N80_MK, 4, 0);
-                    mma_k_loop<true, false>(tmem + KT_COL, sw128_desc(sK, BOX, 1024), 0,
-                                            sw128_desc(sID, 0, 1024), 0, ID_M128N64_MK, 4, 0);
                     mma_commit(smem_u32(&aux.ek_full));
                     return true;
                 };
@@ -436,7 +427,6 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         float m_cur;  // m[c] at the start of the current chunk
         bool fail = false;
         const float b_lam = p.lambda_in ? 0.f : p.b_lambda[h];
-        uint8_t *dot = smem + CovLayout::DOT;
 
         // ---- C accumulator := C0; chunk 0 operands (C0 snapshot, m / w dot rows)
         {
@@ -461,18 +451,24 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             }
             tmem_st_wait();
             m_cur = p.m0 ? p.m0[(size_t)bh * D + c] : 0.f;
+            // dot rows of both K stages: w (hi, lo) and zero rows; m for chunk 0
             if (qt == 0) {
                 const float w = p.lambda_in ? 0.f : p.w_lambda[(size_t)h * D + c];
                 const float mh = __bfloat162float(__float2bfloat16_rn(m_cur));
                 const float wh = __bfloat162float(__float2bfloat16_rn(w));
-                put_bf16(dot + sw128_off(0, c, 16), mh);
-                put_bf16(dot + sw128_off(1, c, 16), m_cur - mh);
-                put_bf16(dot + sw128_off(2, c, 16), wh);
-                put_bf16(dot + sw128_off(3, c, 16), w - wh);
+                put_bf16(smem + dot_off(0, 0, c), mh);
+                put_bf16(smem + dot_off(0, 1, c), m_cur - mh);
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    put_bf16(smem + dot_off(s, 2, c), wh);
+                    put_bf16(smem + dot_off(s, 3, c), w - wh);
+                }
             } else {
 #pragma unroll
-                for (int row = 0; row < 4; ++row)
-                    put_bf16(dot + sw128_off(4 * qt + row, c, 16), 0.f);
+                for (int s = 0; s < 2; ++s)
+#pragma unroll
+                    for (int row = 0; row < 4; ++row)
+                        put_bf16(smem + dot_off(s, 4 * qt + row, c), 0.f);
             }
             tc_fence_before();
             fence_async_smem();
@@ -571,10 +567,10 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                             store8(c0n + sw128_chunk(c, 32 * qt + 16 * hb + 8 * g, 128), v);
                         }
                     }
-                    if (qt == 0) {
+                    if (qt == 0) {  // m rows of the next chunk's K stage
                         const float mh = __bfloat162float(__float2bfloat16_rn(m_next));
-                        put_bf16(dot + sw128_off(0, c, 16), mh);
-                        put_bf16(dot + sw128_off(1, c, 16), m_next - mh);
+                        put_bf16(smem + dot_off(b ^ 1, 0, c), mh);
+                        put_bf16(smem + dot_off(b ^ 1, 1, c), m_next - mh);
                     }
                 }
             }
@@ -588,18 +584,22 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             }
 
             // ---- cleaned, decay-scaled query Qt^T (thread = channel c, 16 tokens)
-            ok = wait_all(smem_u32(&aux.p_full[b]), ph2, abort);
+            ok = wait_all(smem_u32(&aux.p_full[b]), ph2, abort) &&
+                 wait_all(smem_u32(&aux.full[b]), ph2, abort);
             tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 8);
             if (ok) {
                 uint8_t *qtb = smem + CovLayout::QT + b * 16384;
+                const uint8_t *sQs = smem + CovLayout::Q + b * TILE;
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     const int i0 = 16 * qt + 8 * g;
-                    uint32_t pr[8], er[8], qr[8];
+                    uint32_t pr[8], er[8];
                     tmem_ld8(tl + P_COL(b) + i0, pr);
                     tmem_ld8(tl + E0_COL + i0, er);
-                    tmem_ld8(tl + QT_COL + i0, qr);
+                    float qv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qv[e] = bf16_at(sQs, i0 + e, c, 64);
                     tmem_ld_wait();
                     if (tid == 0 && g == 0) CCQ_TRACE(0, n, 9);
                     if (i0 == 0 && u2f(er[0]) < -80.f) record_status(p.status, CCQ_ERR_RANGE);
@@ -607,7 +607,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float2 tk = aux.tok[i0 + e];
-                        const float qc = u2f(qr[e]) - tk.x * (u2f(pr[e]) - tk.y * m_cur);
+                        const float qc = qv[e] - tk.x * (u2f(pr[e]) - tk.y * m_cur);
                         v[e] = qc * exp2f(-1.4426950408889634f * u2f(er[e]));
                     }
                     store8(qtb + sw128_chunk(c, i0, 128), v);
@@ -658,16 +658,20 @@ tc_gla_kernel(const __grid_constant__ Args args) {
 
         // Kh^T = (K * exp(E))^T of chunk k from E^T, K^T in TMEM; gamma = exp(R)
         auto kh_phase = [&](int k, float &gam) -> bool {
-            bool ok = wait_all(smem_u32(&aux.ek_full), k & 1, abort);
+            bool ok = wait_all(smem_u32(&aux.ek_full), k & 1, abort) &&
+                      wait_all(smem_u32(&aux.full[k & 1]), (k >> 1) & 1, abort);
             // Kh (single buffer) is still read by chunk k-1's S update
             if (k > 0) ok = ok && wait_all(smem_u32(&aux.ds_full), (k - 1) & 1, abort);
             tc_fence_after();
             if (ok) {
                 const int i0 = 16 * qt;
-                uint32_t er[16], kr[16], rr[4];
+                const uint8_t *sKs = smem + GlaLayout::K + (k & 1) * TILE;
+                uint32_t er[16], rr[4];
                 tmem_ld16(tl + E1_COL + i0, er);
-                tmem_ld16(tl + KT_COL + i0, kr);
                 tmem_ld4(tl + E1_COL + 64, rr);
+                float kv[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) kv[j] = bf16_at(sKs, i0 + j, c, 64);
                 tmem_ld_wait();
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
@@ -675,7 +679,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int j = 8 * g + e;
-                        v[e] = u2f(kr[j]) * exp2f(1.4426950408889634f * u2f(er[j]));
+                        v[e] = kv[j] * exp2f(1.4426950408889634f * u2f(er[j]));
                     }
                     store8(smem + GlaLayout::KH + sw128_chunk(c, i0 + 8 * g, 128), v);
                 }
