@@ -241,7 +241,8 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         aux.abort = 0;
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&aux.full[s]), 1);
-            mbar_init(smem_u32(&aux.empty[s]), 1);
+            // CTA 0's element-wise threads also read the Q tile of a stage
+            mbar_init(smem_u32(&aux.empty[s]), rank == 0 ? 2 : 1);
             mbar_init(smem_u32(&aux.p_full[s]), 1);
             mbar_init(smem_u32(&aux.qt_empty[s]), 1);
             mbar_init(smem_u32(&aux.qt_full[s]), 1);
@@ -619,6 +620,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (tid == 0) {
                 CCQ_TRACE(0, n, 10);
                 mbar_arrive(smem_u32(&aux.eq_free));
+                mbar_arrive(smem_u32(&aux.empty[b]));  // done reading this stage's Q tile
                 bool sent = true;
                 if (n >= 2)
                     sent = mbar_wait(smem_u32(&aux.qt_empty[b]), ((n >> 1) - 1) & 1, abort, true);
