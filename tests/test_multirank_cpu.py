@@ -1,0 +1,57 @@
+"""Multi-rank host logic of bench.py on CPU (gloo, world size 2).
+
+The CCQ forward shards by (batch, head) with no exchange, so N-GPU runs are
+independent replicas; the only cross-rank logic is the barrier and the
+max-over-ranks of the timed interval.  This runs it with two gloo ranks.
+"""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    import bench  # noqa: WPS433  (imported inside the child on purpose)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        bench.barrier(world)
+        t = bench.max_over_ranks(1.5 + rank, world)
+        out[rank] = t
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.skipif(not dist.is_gloo_available(), reason="gloo backend not built")
+def test_max_over_ranks_with_two_gloo_ranks():
+    world = 2
+    mgr = mp.get_context("spawn").Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(world, _free_port(), out), nprocs=world, join=True,
+                       start_method="spawn")
+    assert dict(out) == {0: 2.5, 1: 2.5}
+
+
+def test_single_rank_is_identity():
+    import bench
+    assert bench.max_over_ranks(3.25, 1) == 3.25
+
+
+def test_flop_and_byte_formulas():
+    import bench
+    # 8 L d + 8 d^2 at L = 64, d = 128
+    assert bench.flops_per_head_token(128) == 8 * 64 * 128 + 8 * 128 * 128 == 196608
+    # q, k, v, log alpha read and o written, bf16
+    assert bench.bytes_per_head_token(128) == 1280
