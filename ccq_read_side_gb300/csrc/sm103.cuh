@@ -31,13 +31,17 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
                  : "memory");
 }
 // Arrive on an mbarrier of another CTA of the cluster (address from mapa).
+// Relaxed: these signals publish no data written by generic stores (the
+// peer's consumers read only what the bulk-copy engine delivered, or only
+// learn that a buffer may be overwritten), so no cluster-scope release fence
+// is needed -- and that fence costs hundreds of cycles.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar)
                  : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t remote_bar, uint32_t bytes) {
     asm volatile(
-        "mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
+        "mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
             remote_bar),
         "r"(bytes)
         : "memory");
