@@ -30,6 +30,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 WORKLOAD_INDEX = 2          # B4 H16 T4096 d128 bf16, anisotropic keys + needle
+METRIC = "CCQ-GLA fwd tokens/s & TFLOP/s (frac of bf16 peak), H16 d128 T4K, 1xGB300"
 L_FLOP = 64                 # chunk length the FLOP count is fixed at
 
 
@@ -43,6 +44,20 @@ def flops_per_head_token(d: int, L: int = L_FLOP) -> int:
 def bytes_per_head_token(d: int, elem: int = 2) -> int:
     """Algorithmic HBM bytes per head-token: q, k, v, log_alpha read, o written."""
     return 5 * d * elem
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the tensor-core kernel from the committed
+    Nsight Compute capture, or None if the kernel source changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "tc_gla_traffic.json")
+    if not os.path.exists(path):
+        return None
+    j = json.load(open(path))
+    h = hashlib.sha256()
+    for f in j["source_files"]:
+        h.update(open(os.path.join(ROOT, f), "rb").read())
+    return j["bytes_per_launch"] if h.hexdigest()[:16] == j["source_sha256_16"] else None
 
 
 def load_peaks():
@@ -186,7 +201,7 @@ def run_reference(args, world, rank):
     value = statistics.mean(v[0]["value"] for v in vals)
     cb = dict(vals[-1][0])
     cb["value"] = value
-    line = {"impl": "reference", "metric": "CCQ-GLA fwd tokens/s", "value": value,
+    line = {"impl": "reference", "metric": METRIC, "value": value,
             "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": statistics.mean(v[1] for v in vals) * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -286,7 +301,7 @@ def run_ours(args, world, rank, local):
     if rank != 0:
         return
     line = {
-        "metric": "CCQ-GLA fwd tokens/s & TFLOP/s (frac of bf16 peak), H16 d128 T4K, 1xGB300",
+        "metric": METRIC,
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -299,7 +314,8 @@ def run_ours(args, world, rank, local):
         "flop_formula": "(8*L*d + 8*d^2) per head-token, L=64, d=128",
         "head_tokens_per_s": head_tokens * world / t_step,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm_peak, "traffic": None,
+                     "frac": achieved_gbs / hbm_peak, "traffic": profiled_traffic(),
+                     "traffic_unit": "bytes per launch",
                      "peak_source": f"{src} hbm_gbs (copy)",
                      "tensor": {"achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s",
                                 "frac": tflops / bf16_peak,
