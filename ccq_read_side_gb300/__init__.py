@@ -17,13 +17,14 @@ from typing import Dict, Optional, Tuple
 import torch
 
 __all__ = ["gla_fwd", "gdn_fwd", "last_device_status", "status_string", "CcqError",
-           "library", "FLAG_L2NORM_QK", "FLAG_FP32_PATH", "STATUS"]
+           "library", "FLAG_L2NORM_QK", "FLAG_FP32_PATH", "FLAG_TEST_STALL", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libccq.so")
 
 FLAG_L2NORM_QK = 1
 FLAG_FP32_PATH = 2
+FLAG_TEST_STALL = 0x100  # test only: makes the tensor-core kernel's bounded waits run out
 STATUS = {0: "CCQ_OK", 1: "CCQ_ERR_INVALID_ARG", 2: "CCQ_ERR_UNSUPPORTED", 3: "CCQ_ERR_CUDA",
           4: "CCQ_ERR_TIMEOUT", 5: "CCQ_ERR_RANGE"}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}

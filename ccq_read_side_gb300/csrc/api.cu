@@ -40,7 +40,8 @@ static ccq_status check_common(const CcqParams &p, ccq_dtype dtype) {
     if (given == 0 && p.t0 != 0) return CCQ_ERR_INVALID_ARG;
     if (dtype != CCQ_DTYPE_F32 && dtype != CCQ_DTYPE_BF16) return CCQ_ERR_UNSUPPORTED;
     if ((p.dk != 64 && p.dk != 128) || (p.dv != 64 && p.dv != 128)) return CCQ_ERR_UNSUPPORTED;
-    if (p.flags & ~(CCQ_FLAG_L2NORM_QK | CCQ_FLAG_FP32_PATH)) return CCQ_ERR_INVALID_ARG;
+    if (p.flags & ~(CCQ_FLAG_L2NORM_QK | CCQ_FLAG_FP32_PATH | CCQ_FLAG_TEST_STALL))
+        return CCQ_ERR_INVALID_ARG;
     if ((long long)p.B * p.H > 0x7fffffffLL) return CCQ_ERR_UNSUPPORTED;
     if ((long long)p.T + p.t0 > (1LL << 40)) return CCQ_ERR_UNSUPPORTED;
     return CCQ_OK;
@@ -71,8 +72,11 @@ extern "C" ccq_status ccq_gla_fwd(const void *q, const void *k, const void *v,
     if (!p.status) return CCQ_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const bool bf16 = dtype == CCQ_DTYPE_BF16;
-    if (bf16 && !(flags & CCQ_FLAG_FP32_PATH) && tc_gla_supported(p))
-        return to_status(launch_tc_gla(p, st));
+    const bool tc = bf16 && !(flags & CCQ_FLAG_FP32_PATH) && tc_gla_supported(p);
+    if (flags & CCQ_FLAG_TEST_STALL) {
+        if (!tc) return CCQ_ERR_UNSUPPORTED;
+    }
+    if (tc) return to_status(launch_tc_gla(p, st));
     return to_status(launch_simt(p, false, bf16, st));
 }
 
@@ -90,6 +94,7 @@ extern "C" ccq_status ccq_gdn_fwd(const void *q, const void *k, const void *v,
     ccq_status s = check_common(p, dtype);
     if (s != CCQ_OK) return s;
     if (!beta && T > 0 && B > 0 && H > 0) return CCQ_ERR_INVALID_ARG;
+    if (flags & CCQ_FLAG_TEST_STALL) return CCQ_ERR_UNSUPPORTED;  // GLA tensor-core kernel only
     p.status = status_word();
     if (!p.status) return CCQ_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -302,7 +302,9 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             const uint32_t base1 = rank == 0 ? CovLayout::K : GlaLayout::LA;
             const uint32_t base2 = rank == 0 ? CovLayout::LA : GlaLayout::V;
             const uint32_t stage1 = rank == 0 ? KTILE : TILE, blk1 = rank == 0 ? KBLK : BOX;
-            for (int n = 0; n < nch; ++n) {
+            // (test mode: no loads, so every consumer's bounded wait runs out)
+            const int nload = (p.flags & CCQ_FLAG_TEST_STALL) ? 0 : nch;
+            for (int n = 0; n < nload; ++n) {
                 const int s = n & 1;
                 if (n >= 2 && !mbar_wait(smem_u32(&aux.empty[s]), ((n >> 1) - 1) & 1, abort))
                     break;

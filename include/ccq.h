@@ -82,6 +82,11 @@ typedef enum { CCQ_DTYPE_F32 = 0, CCQ_DTYPE_BF16 = 1 } ccq_dtype;
 
 #define CCQ_FLAG_L2NORM_QK 1u  /* normalise q and k by 1/sqrt(|x|^2 + 1e-6) before use */
 #define CCQ_FLAG_FP32_PATH 2u  /* force the fp32 CUDA-core kernel (any dtype/shape) */
+/* Test only (failure detection): the tensor-core kernel issues no input loads,
+ * so its bounded waits run out after a few seconds and the call records
+ * CCQ_ERR_TIMEOUT without faulting or hanging the GPU.  Requires a shape the
+ * tensor-core kernel takes (bf16, dk = dv = 128), else CCQ_ERR_UNSUPPORTED. */
+#define CCQ_FLAG_TEST_STALL 0x100u
 
 /*
  * CCQ forward on the GLA backbone (definitions above).

@@ -1,0 +1,44 @@
+"""Failure detection on the GPU without a GPU fault: the tensor-core kernel's
+waits are bounded; with the test-only stall flag nothing feeds them, so they
+run out, the call records CCQ_ERR_TIMEOUT in the device status word, and the
+context stays usable for the next (checked) call."""
+import numpy as np
+import pytest
+import torch
+
+import ccq_read_side_gb300 as ccq
+import oracle
+from ccq_read_side_gb300.workloads import Workload, make_inputs
+from parity import check, np64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs():
+    return make_inputs(Workload("stall", "gla", "bf16", 1, 2, 100, 128, 128, 64, 21, "iso"))
+
+
+def test_bounded_waits_report_timeout_and_context_survives():
+    inp = _inputs()
+    d = to_dev(inp)
+    assert ccq.last_device_status() == 0
+    ccq.gla_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["w_lambda"], d["b_lambda"],
+                flags=ccq.FLAG_TEST_STALL)
+    torch.cuda.synchronize()
+    assert ccq.last_device_status() == 4  # CCQ_ERR_TIMEOUT
+    assert ccq.last_device_status() == 0  # read clears it
+    # the same context runs a normal call correctly afterwards
+    o, st = ccq.gla_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["w_lambda"], d["b_lambda"])
+    torch.cuda.synchronize()
+    assert ccq.last_device_status() == 0
+    ref = oracle.run("gla", inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["w_lambda"],
+                     inp["b_lambda"])
+    check(np64(o), ref["o"], "bf16", "after timeout")
+
+
+def test_stall_flag_rejected_where_no_tensor_core_path():
+    inp = _inputs()
+    d = to_dev(inp)
+    with pytest.raises(ccq.CcqError):
+        ccq.gla_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["w_lambda"], d["b_lambda"],
+                    flags=ccq.FLAG_TEST_STALL | ccq.FLAG_FP32_PATH)
