@@ -103,8 +103,8 @@ __host__ __device__ constexpr uint32_t dot_off(int s, int row, int c) {
 // rows 65-79 are zero.
 
 struct Aux {
-    uint64_t full[2], empty[2];                                                 // TMA stages
-    uint64_t aqk_full, p_full[2], dc_full, c0_ready, ahat_ready, eq_full, eq_free,
+    uint64_t full[2], empty[2];  // TMA stages (empty: CTA 0 only)
+    uint64_t aqk_full, p_full[2], c0_ready, ahat_ready, eq_full, eq_free,
         qt_empty[2];                                                            // CTA 0
     uint64_t qt_full[2], kh_ready, sb_ready, ds_full, stage1, ek_full, ag_ready, o_full[2];  // CTA 1
     uint32_t tmem_base;
@@ -198,24 +198,38 @@ constexpr uint32_t ID_M128N80_MK = idesc_bf16(128, 80, 1, 0);
 constexpr uint32_t ID_M128N16_MK = idesc_bf16(128, 16, 1, 0);
 
 
-// Issues nk MMAs (K = 16 each) into d; the k-th uses operand byte offsets
-// koff(k) on both descriptors' start addresses.  Rolled on purpose: the hot
-// loops of this kernel must fit the instruction cache.
+// Issues nk MMAs (K = 16 each) into d; the k-th uses byte offsets koff(k)
+// on both descriptors' start addresses:
 //   K-major operand, 64-wide K blocks `blk` bytes apart: koff = (k/4)*blk + (k%4)*32
-//   MN-major operand (rows are K): koff = k * 2048
-__device__ __forceinline__ uint32_t koff_k(int k, uint32_t blk) { return (k >> 2) * blk + (k & 3) * 32; }
-__device__ __forceinline__ uint32_t koff_mn(int k) { return (uint32_t)k * 2048u; }
-__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
-
-template <bool A_MN, bool B_MN>
-__device__ __forceinline__ void mma_k_loop(uint32_t d, uint64_t adesc, uint32_t ablk, uint64_t bdesc,
-                                        uint32_t bblk, uint32_t idesc, int nk, uint32_t acc0) {
+//   MN-major operand (rows are K):                       koff = k * 2048
+// One out-of-line routine serves every MMA group of the kernel, so its few
+// instructions stay in the instruction cache while the element-wise warps
+// stream through their (much larger) code; the start-address field sits in
+// the descriptor's low word, so each step is a 32-bit add.
+__device__ __noinline__ void mma_group(uint32_t d, uint32_t a_lo, uint32_t a_hi, uint32_t a_blk,
+                                       uint32_t b_lo, uint32_t b_hi, uint32_t b_blk, uint32_t a_k,
+                                       uint32_t b_k, uint32_t idesc, uint32_t nblk, uint32_t acc0) {
 #pragma unroll 1
-    for (int k = 0; k < nk; ++k) {
-        const uint32_t ao = A_MN ? koff_mn(k) : koff_k(k, ablk);
-        const uint32_t bo = B_MN ? koff_mn(k) : koff_k(k, bblk);
-        mma_bf16(d, desc_add(adesc, ao), desc_add(bdesc, bo), idesc, (k > 0) | acc0);
+    for (uint32_t j = 0; j < nblk; ++j) {
+#pragma unroll
+        for (uint32_t i = 0; i < 4; ++i) {
+            const uint64_t ad = ((uint64_t)a_hi << 32) | (a_lo + i * a_k);
+            const uint64_t bd = ((uint64_t)b_hi << 32) | (b_lo + i * b_k);
+            mma_bf16(d, ad, bd, idesc, (i | j) ? 1u : acc0);
+        }
+        a_lo += a_blk;
+        b_lo += b_blk;
     }
+}
+
+template <bool A_MN, bool B_MN, int NK>
+__device__ __forceinline__ void mma_k_loop(uint32_t d, uint64_t adesc, uint32_t ablk, uint64_t bdesc,
+                                           uint32_t bblk, uint32_t idesc, uint32_t acc0) {
+    static_assert(NK % 4 == 0, "whole 64-wide K blocks");
+    // descriptor units are 16 bytes
+    mma_group(d, (uint32_t)adesc, (uint32_t)(adesc >> 32), A_MN ? 4 * 128 : ablk >> 4,
+              (uint32_t)bdesc, (uint32_t)(bdesc >> 32), B_MN ? 4 * 128 : bblk >> 4,
+              A_MN ? 128 : 2, B_MN ? 128 : 2, idesc, NK / 4, acc0);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
@@ -242,14 +256,13 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(smem_u32(&aux.full[s]), 1);
             // CTA 0's element-wise threads also read the Q tile of a stage
-            mbar_init(smem_u32(&aux.empty[s]), rank == 0 ? 2 : 1);
+            mbar_init(smem_u32(&aux.empty[s]), 1);
             mbar_init(smem_u32(&aux.p_full[s]), 1);
             mbar_init(smem_u32(&aux.qt_empty[s]), 1);
             mbar_init(smem_u32(&aux.qt_full[s]), 1);
             mbar_init(smem_u32(&aux.o_full[s]), 1);
         }
         mbar_init(smem_u32(&aux.aqk_full), 1);
-        mbar_init(smem_u32(&aux.dc_full), 1);
         mbar_init(smem_u32(&aux.c0_ready), 1);
         mbar_init(smem_u32(&aux.ahat_ready), 1);
         mbar_init(smem_u32(&aux.eq_full), 1);
@@ -304,10 +317,24 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             const uint32_t stage1 = rank == 0 ? KTILE : TILE, blk1 = rank == 0 ? KBLK : BOX;
             // (test mode: no loads, so every consumer's bounded wait runs out)
             const int nload = (p.flags & CCQ_FLAG_TEST_STALL) ? 0 : nch;
+            // L2 prefetch runs two chunks ahead of the loads, so a load issued
+            // when its stage frees up finds its tiles in L2
+            auto prefetch = [&](int k) {
+                for (int b = 0; b < 2; ++b) {
+                    tma_prefetch_3d(m0, b * 64, k * L, bh);
+                    tma_prefetch_3d(m1, b * 64, k * L, bh);
+                    tma_prefetch_3d(m2, b * 64, k * L, bh);
+                }
+            };
+            for (int k = 0; k < 2 && k < nload; ++k) prefetch(k);
             for (int n = 0; n < nload; ++n) {
                 const int s = n & 1;
-                if (n >= 2 && !mbar_wait(smem_u32(&aux.empty[s]), ((n >> 1) - 1) & 1, abort))
-                    break;
+                if (n + 2 < nload) prefetch(n + 2);
+                // stage s is free once chunk n-2 is done with it: CTA 0 -- its
+                // element-wise threads say so (they read the Q tile last); CTA 1 --
+                // the chunk's last MMA group has completed (o_full of chunk n-2)
+                const uint32_t rel = rank == 0 ? smem_u32(&aux.empty[s]) : smem_u32(&aux.o_full[s]);
+                if (n >= 2 && !mbar_wait(rel, ((n >> 1) - 1) & 1, abort)) break;
                 CCQ_TRACE(2, n, 0);
                 const uint32_t fb = smem_u32(&aux.full[s]);
                 mbar_expect_tx(fb, 3 * TILE);
@@ -340,36 +367,37 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     tc_fence_after();
                     CCQ_TRACE(1, n, 1);
                     // [A | m_hi.q m_lo.q w_hi.q w_lo.q] = Q [K | dot rows]^T
-                    mma_k_loop<false, false>(tmem + AQK_COL, sw128_desc(sQ, 0, 1024), BOX,
-                                             sw128_desc(sK, 0, 1024), KBLK, ID_M64N80_KK, 8, 0);
+                    mma_k_loop<false, false, 8>(tmem + AQK_COL, sw128_desc(sQ, 0, 1024), BOX,
+                                             sw128_desc(sK, 0, 1024), KBLK, ID_M64N80_KK, 0);
                     mma_commit(smem_u32(&aux.aqk_full));
+                    CCQ_TRACE(1, n, 6);
                     const uint32_t sC0 = smem_u32(smem + CovLayout::C0 + b * 32768);
                     // P^T = C0 Q^T
-                    mma_k_loop<false, false>(tmem + P_COL(b), sw128_desc(sC0, 0, 1024), 16384,
-                                             sw128_desc(sQ, 0, 1024), BOX, ID_M128N64_KK, 8, 0);
+                    mma_k_loop<false, false, 8>(tmem + P_COL(b), sw128_desc(sC0, 0, 1024), 16384,
+                                             sw128_desc(sQ, 0, 1024), BOX, ID_M128N64_KK, 0);
+                    CCQ_TRACE(1, n, 7);
                     // C += K^T K
-                    mma_k_loop<true, true>(tmem + C_COL, sw128_desc(sK, KBLK, 1024), 0,
-                                           sw128_desc(sK, KBLK, 1024), 0, ID_M128N128_MM, 4, 1);
-                    mma_commit(smem_u32(&aux.dc_full));
+                    mma_k_loop<true, true, 4>(tmem + C_COL, sw128_desc(sK, KBLK, 1024), 0,
+                                           sw128_desc(sK, KBLK, 1024), 0, ID_M128N128_MM, 1);
+                    CCQ_TRACE(1, n, 8);
                     if (n > 0 && !mbar_wait(smem_u32(&aux.eq_free), (n - 1) & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 5);
                     // E^T = LA^T U^T, colsum(K)
-                    mma_k_loop<true, false>(tmem + E0_COL, sw128_desc(sLA, BOX, 1024), 0,
-                                            sw128_desc(sUX, 0, 1024), 0, ID_M128N64_MK, 4, 0);
-                    mma_k_loop<true, false>(tmem + KS_COL, sw128_desc(sK, KBLK, 1024), 0,
-                                            sw128_desc(sUX + 64 * 128, 0, 1024), 0, ID_M128N16_MK,
-                                            4, 0);
+                    mma_k_loop<true, false, 4>(tmem + E0_COL, sw128_desc(sLA, BOX, 1024), 0,
+                                            sw128_desc(sUX, 0, 1024), 0, ID_M128N64_MK, 0);
+                    mma_k_loop<true, false, 4>(tmem + KS_COL, sw128_desc(sK, KBLK, 1024), 0,
+                                            sw128_desc(sUX + 64 * 128, 0, 1024), 0, ID_M128N16_MK, 0);
                     mma_commit(smem_u32(&aux.eq_full));
+                    CCQ_TRACE(1, n, 9);
                     if (!mbar_wait(smem_u32(&aux.ahat_ready), n & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 2);
                     const uint32_t sAH = smem_u32(smem + CovLayout::AH);
                     // P^T += K^T Ah^T
-                    mma_k_loop<true, false>(tmem + P_COL(b), sw128_desc(sK, KBLK, 1024), 0,
-                                            sw128_desc(sAH, 0, 1024), 0, ID_M128N64_MK, 4, 1);
+                    mma_k_loop<true, false, 4>(tmem + P_COL(b), sw128_desc(sK, KBLK, 1024), 0,
+                                            sw128_desc(sAH, 0, 1024), 0, ID_M128N64_MK, 1);
                     mma_commit(smem_u32(&aux.p_full[b]));
-                    mma_commit(smem_u32(&aux.empty[s]));
                     CCQ_TRACE(1, n, 3);
                 }
             } else {
@@ -379,9 +407,12 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     if (!mbar_wait(smem_u32(&aux.full[s]), (k >> 1) & 1, abort)) return false;
                     tc_fence_after();
                     const uint32_t sLA = smem_u32(smem + GlaLayout::LA + s * TILE);
-                    mma_k_loop<true, false>(tmem + E1_COL, sw128_desc(sLA, BOX, 1024), 0,
-                                            sw128_desc(sUX, 0, 1024), 0, ID_M128N80_MK, 4, 0);
-                    mma_commit(smem_u32(&aux.ek_full));
+                    mma_k_loop<true, false, 4>(tmem + E1_COL, sw128_desc(sLA, BOX, 1024), 0,
+                                            sw128_desc(sUX, 0, 1024), 0, ID_M128N80_MK, 0);
+                    // chunk 0 has its own signal; later chunks' E^T are issued
+                    // ahead of the previous chunk's first group and covered by
+                    // its commit (stage1)
+                    if (k == 0) mma_commit(smem_u32(&aux.ek_full));
                     return true;
                 };
                 if (nch > 0 && issue_ek(0)) {
@@ -394,31 +425,35 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                         const uint32_t sAG = smem_u32(smem + GlaLayout::AG);
                         const uint32_t sQT = smem_u32(smem + GlaLayout::QTR + b * 16384);
                         if (!mbar_wait(smem_u32(&aux.kh_ready), n & 1, abort)) break;
+                        // E^T of chunk n has been read: the next chunk's E^T may
+                        // overwrite it while the element-wise warps build Sb
+                        if (n + 1 < nch && !issue_ek(n + 1)) break;
                         if (!mbar_wait(smem_u32(&aux.sb_ready), n & 1, abort)) break;
                         CCQ_TRACE(1, n, 0);
                         if (!mbar_wait(smem_u32(&aux.qt_full[b]), ph2, abort, true)) break;
                         tc_fence_after();
                         CCQ_TRACE(1, n, 1);
                         // Ag = Qt Kh^T (channel-major operands)
-                        mma_k_loop<true, true>(tmem + AG_COL, sw128_desc(sQT, 16384, 1024), 0,
-                                               sw128_desc(sKH, 16384, 1024), 0, ID_M64N64_MM, 8, 0);
+                        mma_k_loop<true, true, 8>(tmem + AG_COL, sw128_desc(sQT, 16384, 1024), 0,
+                                               sw128_desc(sKH, 16384, 1024), 0, ID_M64N64_MM, 0);
+                        CCQ_TRACE(1, n, 6);
                         // O^T = Sb^T Qt^T
-                        mma_k_loop<true, true>(tmem + O_COL(b), sw128_desc(sSB, 16384, 1024), 0,
-                                               sw128_desc(sQT, 16384, 1024), 0, ID_M128N64_MM, 8, 0);
+                        mma_k_loop<true, true, 8>(tmem + O_COL(b), sw128_desc(sSB, 16384, 1024), 0,
+                                               sw128_desc(sQT, 16384, 1024), 0, ID_M128N64_MM, 0);
                         mma_commit(smem_u32(&aux.stage1));
+                        CCQ_TRACE(1, n, 7);
                         // S = Sb + Kh^T V (Sb already in TMEM)
-                        mma_k_loop<false, true>(tmem + S_COL, sw128_desc(sKH, 0, 1024), 0,
-                                                sw128_desc(sV, BOX, 1024), 0, ID_M128N128_KM, 4, 1);
+                        mma_k_loop<false, true, 4>(tmem + S_COL, sw128_desc(sKH, 0, 1024), 0,
+                                                sw128_desc(sV, BOX, 1024), 0, ID_M128N128_KM, 1);
                         mma_commit(smem_u32(&aux.ds_full));
-                        if (n + 1 < nch && !issue_ek(n + 1)) break;
+                        CCQ_TRACE(1, n, 8);
                         if (!mbar_wait(smem_u32(&aux.ag_ready), n & 1, abort)) break;
                         tc_fence_after();
                         CCQ_TRACE(1, n, 2);
                         // O^T += V^T Ag^T
-                        mma_k_loop<true, false>(tmem + O_COL(b), sw128_desc(sV, BOX, 1024), 0,
-                                                sw128_desc(sAG, 0, 1024), 0, ID_M128N64_MK, 4, 1);
+                        mma_k_loop<true, false, 4>(tmem + O_COL(b), sw128_desc(sV, BOX, 1024), 0,
+                                                sw128_desc(sAG, 0, 1024), 0, ID_M128N64_MK, 1);
                         mma_commit(smem_u32(&aux.o_full[b]));
-                        mma_commit(smem_u32(&aux.empty[s]));
                         CCQ_TRACE(1, n, 3);
                     }
                 }
@@ -545,8 +580,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
 
             // ---- next chunk's operands: C0 snapshot (C accumulator after dC_n), m += colsum K_n
             ok = wait_all(smem_u32(&aux.eq_full), n & 1, abort);
-            if (more) ok = ok && wait_all(smem_u32(&aux.dc_full), n & 1, abort);
-            tc_fence_after();
+                        tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 5);
             float m_next = m_cur;
             if (ok) {
@@ -622,7 +656,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (tid == 0) {
                 CCQ_TRACE(0, n, 10);
                 mbar_arrive(smem_u32(&aux.eq_free));
-                mbar_arrive(smem_u32(&aux.empty[b]));  // done reading this stage's Q tile
+                mbar_arrive(smem_u32(&aux.empty[b]));  // stage b: MMAs done (p_full), Q tile read
                 bool sent = true;
                 if (n >= 2)
                     sent = mbar_wait(smem_u32(&aux.qt_empty[b]), ((n >> 1) - 1) & 1, abort, true);
@@ -640,7 +674,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         }
         // ---- final state: C (TMEM accumulator), m
         if (!fail && nch > 0) {
-            const bool ok = wait_all(smem_u32(&aux.dc_full), (nch - 1) & 1, abort);
+            const bool ok = wait_all(smem_u32(&aux.eq_full), (nch - 1) & 1, abort);
             tc_fence_after();
             if (ok && p.C_out) {
                 uint32_t cr[32];
@@ -662,11 +696,14 @@ tc_gla_kernel(const __grid_constant__ Args args) {
 
         // Kh^T = (K * exp(E))^T of chunk k from E^T, K^T in TMEM; gamma = exp(R)
         auto kh_phase = [&](int k, float &gam) -> bool {
-            bool ok = wait_all(smem_u32(&aux.ek_full), k & 1, abort) &&
+            // E^T of chunk k > 0 was committed with chunk k-1's first MMA group
+            // (stage1), which every element-wise thread has already waited for
+            bool ok = (k > 0 || wait_all(smem_u32(&aux.ek_full), 0, abort)) &&
                       wait_all(smem_u32(&aux.full[k & 1]), (k >> 1) & 1, abort);
             // Kh (single buffer) is still read by chunk k-1's S update
             if (k > 0) ok = ok && wait_all(smem_u32(&aux.ds_full), (k - 1) & 1, abort);
             tc_fence_after();
+            if (tid == 0 && k > 0) CCQ_TRACE(0, k - 1, 6);
             if (ok) {
                 const int i0 = 16 * qt;
                 const uint8_t *sKs = smem + GlaLayout::K + (k & 1) * TILE;
@@ -677,6 +714,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) kv[j] = bf16_at(sKs, i0 + j, c, 64);
                 tmem_ld_wait();
+                if (tid == 0 && k > 0) CCQ_TRACE(0, k - 1, 7);
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     float v[8];
@@ -691,9 +729,11 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 if (qt == 0 && R < -80.f) record_status(p.status, CCQ_ERR_RANGE);
                 gam = exp2f(1.4426950408889634f * R);
             }
+            if (tid == 0 && k > 0) CCQ_TRACE(0, k - 1, 8);
             tc_fence_before();
             fence_async_smem();
             if (epi_sync_any(!ok)) return false;
+            if (tid == 0 && k > 0) CCQ_TRACE(0, k - 1, 9);
             if (tid == 0) mbar_arrive(smem_u32(&aux.kh_ready));
             return true;
         };
@@ -708,6 +748,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     tmem_ld32(tl + S_COL + 32 * qt, sr);
                     tmem_ld_wait();
                 }
+                if (tid == 0) CCQ_TRACE(0, k - 1, 10);
             } else {
                 const float *src = p.S0 ? p.S0 + ((size_t)bh * D + c) * D + 32 * qt : nullptr;
 #pragma unroll
@@ -736,6 +777,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             tc_fence_before();
             fence_async_smem();
             if (epi_sync_any(!ok)) return false;
+            if (tid == 0 && k > 0) CCQ_TRACE(0, k - 1, 11);
             if (tid == 0) mbar_arrive(smem_u32(&aux.sb_ready));
             return true;
         };
@@ -784,6 +826,10 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             if (n + 1 < nch && !kh_phase(n + 1, gam_next)) { fail = true; break; }
             if (tid == 0) CCQ_TRACE(0, n, 3);
 
+            // ---- next chunk's Sb snapshot (chunk n's S update is issued before
+            // the last O MMA, so this overlaps it)
+            if (n + 1 < nch && !sb_phase(n + 1, gam_next)) { fail = true; break; }
+
             // ---- output tile (O^T: lane = d_v channel, columns = tokens)
             ok = wait_all(smem_u32(&aux.o_full[b]), ph2, abort);
             tc_fence_after();
@@ -807,8 +853,6 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 CCQ_TRACE(0, n, 5);
             }
 
-            // ---- next chunk's Sb snapshot
-            if (n + 1 < nch && !sb_phase(n + 1, gam_next)) { fail = true; break; }
         }
         // ---- final state S (TMEM accumulator)
         if (!fail && nch > 0 && p.S_out) {
