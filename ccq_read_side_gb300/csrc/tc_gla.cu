@@ -21,12 +21,15 @@
 //   the chunk's tokens after i, and Qt^T (16 KB) goes to CTA 1 through
 //   distributed shared memory (asynchronous bulk copy, double-buffered).
 //
-//   Column-wise quantities that the element-wise threads (one lane per
-//   channel) would otherwise gather one bf16 at a time also come from the
-//   tensor core, exactly (bf16 inputs, fp32 accumulation): the suffix sums
-//   E^T = LA^T U^T with U the strictly-upper ones matrix (plus a ones row for
-//   the chunk total R), Q^T and K^T through an identity, and colsum(K)
-//   through a ones row.
+//   The per-channel suffix sums of log alpha come from the tensor core,
+//   exactly (bf16 inputs, fp32 accumulation): E^T = LA^T U^T with U the
+//   strictly-upper ones matrix (plus a ones row for the chunk total R).
+//   colsum(K), which advances m, is summed by the element-wise threads from
+//   the K tile while they wait for A.
+//
+//   Per chunk CTA 0 has three element-wise phases and two MMA commits: the
+//   m rows for the next chunk's Q K^T are ready after the gate phase, the
+//   next C0 snapshot after the query phase.
 //
 //   CTA 1 ("GLA side") owns S (fp32 accumulator in tensor memory).  With
 //   Kh = K * exp(E) and Sb = Diag(exp R) S (R = the chunk's total log-decay):
@@ -103,14 +106,15 @@ __host__ __device__ constexpr uint32_t dot_off(int s, int row, int c) {
 // rows 65-79 are zero.
 
 struct Aux {
-    uint64_t full[2], empty[2];  // TMA stages (empty: CTA 0 only)
-    uint64_t aqk_full, p_full[2], c0_ready, ahat_ready, eq_full, eq_free,
-        qt_empty[2];                                                            // CTA 0
+    uint64_t full[2], empty[2];  // TMA stages (CTA 1: K and log alpha; V below)
+    uint64_t vfull[2];           // CTA 1: V tile of a stage
+    uint64_t aqk_full, p_full[2], m_ready, c0_ready, ahat_ready, qt_empty[2];  // CTA 0
     uint64_t qt_full[2], kh_ready, sb_ready, ds_full, stage1, ek_full, ag_ready, o_full[2];  // CTA 1
     uint32_t tmem_base;
     int abort;
     float2 tok[L];            // CTA 0: (lambda_i / t_i, s_i / t_i)
     float part[4][L];         // CTA 0: row-sum quarters
+    float kpart[4][D];        // CTA 0: column sums of K, quarters of the chunk
 };
 constexpr size_t SMEM_BYTES = 1024 + TILES_END + sizeof(Aux);
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -120,7 +124,6 @@ constexpr uint32_t C_COL = 0;      // CTA 0: C accumulator (128)
 constexpr uint32_t AQK_COL = 128;  //        A (64) + dots (16)
 __host__ __device__ constexpr uint32_t P_COL(int b) { return 224 + 64 * b; }
 constexpr uint32_t E0_COL = 352;   //        E^T (64)
-constexpr uint32_t KS_COL = 480;   //        colsum(K) (16)
 constexpr uint32_t S_COL = 0;      // CTA 1: S accumulator (128)
 constexpr uint32_t AG_COL = 128;   //        Ag (64)
 __host__ __device__ constexpr uint32_t O_COL(int b) { return 192 + 64 * b; }
@@ -186,7 +189,6 @@ __device__ __forceinline__ bool wait_all(uint32_t bar, uint32_t parity, volatile
 }
 
 // Instruction descriptors (bf16 x bf16 -> fp32); K = K-major, M = MN-major.
-constexpr uint32_t ID_M64N64_KK = idesc_bf16(64, 64, 0, 0);
 constexpr uint32_t ID_M64N80_KK = idesc_bf16(64, 80, 0, 0);
 constexpr uint32_t ID_M64N64_MM = idesc_bf16(64, 64, 1, 1);
 constexpr uint32_t ID_M128N64_KK = idesc_bf16(128, 64, 0, 0);
@@ -195,7 +197,6 @@ constexpr uint32_t ID_M128N64_MM = idesc_bf16(128, 64, 1, 1);
 constexpr uint32_t ID_M128N128_MM = idesc_bf16(128, 128, 1, 1);
 constexpr uint32_t ID_M128N128_KM = idesc_bf16(128, 128, 0, 1);
 constexpr uint32_t ID_M128N80_MK = idesc_bf16(128, 80, 1, 0);
-constexpr uint32_t ID_M128N16_MK = idesc_bf16(128, 16, 1, 0);
 
 
 // Issues nk MMAs (K = 16 each) into d; the k-th uses byte offsets koff(k)
@@ -261,12 +262,12 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             mbar_init(smem_u32(&aux.qt_empty[s]), 1);
             mbar_init(smem_u32(&aux.qt_full[s]), 1);
             mbar_init(smem_u32(&aux.o_full[s]), 1);
+            mbar_init(smem_u32(&aux.vfull[s]), 1);
         }
         mbar_init(smem_u32(&aux.aqk_full), 1);
         mbar_init(smem_u32(&aux.c0_ready), 1);
         mbar_init(smem_u32(&aux.ahat_ready), 1);
-        mbar_init(smem_u32(&aux.eq_full), 1);
-        mbar_init(smem_u32(&aux.eq_free), 1);
+        mbar_init(smem_u32(&aux.m_ready), 1);
         mbar_init(smem_u32(&aux.kh_ready), 1);
         mbar_init(smem_u32(&aux.sb_ready), 1);
         mbar_init(smem_u32(&aux.ds_full), 1);
@@ -330,21 +331,30 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             for (int n = 0; n < nload; ++n) {
                 const int s = n & 1;
                 if (n + 2 < nload) prefetch(n + 2);
-                // stage s is free once chunk n-2 is done with it: CTA 0 -- its
-                // element-wise threads say so (they read the Q tile last); CTA 1 --
-                // the chunk's last MMA group has completed (o_full of chunk n-2)
-                const uint32_t rel = rank == 0 ? smem_u32(&aux.empty[s]) : smem_u32(&aux.o_full[s]);
-                if (n >= 2 && !mbar_wait(rel, ((n >> 1) - 1) & 1, abort)) break;
+                // Stage s is free once chunk n-2 is done with it.  CTA 0: its
+                // element-wise threads say so (they read the Q tile last).  CTA 1:
+                // K and log alpha are released by the element-wise threads once
+                // Kh is built; V once the chunk's last MMA group has completed
+                // (o_full), so the next E^T never waits for V's consumers.
+                if (n >= 2 && !mbar_wait(smem_u32(&aux.empty[s]), ((n >> 1) - 1) & 1, abort)) break;
                 CCQ_TRACE(2, n, 0);
                 const uint32_t fb = smem_u32(&aux.full[s]);
-                mbar_expect_tx(fb, 3 * TILE);
+                mbar_expect_tx(fb, (rank == 0 ? 3 : 2) * TILE);
                 for (int b = 0; b < 2; ++b) {
                     tma_load_3d(smem_u32(smem + s * TILE + b * BOX), m0, fb, b * 64, n * L, bh);
                     tma_load_3d(smem_u32(smem + base1 + s * stage1 + b * blk1), m1, fb, b * 64,
                                 n * L, bh);
-                    tma_load_3d(smem_u32(smem + base2 + s * TILE + b * BOX), m2, fb, b * 64,
-                                n * L, bh);
                 }
+                uint32_t f2 = fb;
+                if (rank == 1) {
+                    if (n >= 2 && !mbar_wait(smem_u32(&aux.o_full[s]), ((n >> 1) - 1) & 1, abort))
+                        break;
+                    f2 = smem_u32(&aux.vfull[s]);
+                    mbar_expect_tx(f2, TILE);
+                }
+                for (int b = 0; b < 2; ++b)
+                    tma_load_3d(smem_u32(smem + base2 + s * TILE + b * BOX), m2, f2, b * 64, n * L,
+                                bh);
             }
         }
         __syncwarp();
@@ -362,41 +372,39 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     if (!mbar_wait(smem_u32(&aux.full[s]), ph2, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 0);
-                    CCQ_TRACE(1, n, 4);
-                    if (!mbar_wait(smem_u32(&aux.c0_ready), n & 1, abort)) break;
+                    // the m dot rows of this stage are in place (and A of the
+                    // previous chunk has been read)
+                    if (!mbar_wait(smem_u32(&aux.m_ready), n & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 1);
                     // [A | m_hi.q m_lo.q w_hi.q w_lo.q] = Q [K | dot rows]^T
                     mma_k_loop<false, false, 8>(tmem + AQK_COL, sw128_desc(sQ, 0, 1024), BOX,
-                                             sw128_desc(sK, 0, 1024), KBLK, ID_M64N80_KK, 0);
+                                                sw128_desc(sK, 0, 1024), KBLK, ID_M64N80_KK, 0);
                     mma_commit(smem_u32(&aux.aqk_full));
                     CCQ_TRACE(1, n, 6);
+                    // the C0 snapshot of this chunk is written (so C may advance)
+                    // and the previous chunk's E^T has been read
+                    if (!mbar_wait(smem_u32(&aux.c0_ready), n & 1, abort)) break;
+                    tc_fence_after();
+                    CCQ_TRACE(1, n, 5);
                     const uint32_t sC0 = smem_u32(smem + CovLayout::C0 + b * 32768);
                     // P^T = C0 Q^T
                     mma_k_loop<false, false, 8>(tmem + P_COL(b), sw128_desc(sC0, 0, 1024), 16384,
-                                             sw128_desc(sQ, 0, 1024), BOX, ID_M128N64_KK, 0);
-                    CCQ_TRACE(1, n, 7);
+                                                sw128_desc(sQ, 0, 1024), BOX, ID_M128N64_KK, 0);
                     // C += K^T K
                     mma_k_loop<true, true, 4>(tmem + C_COL, sw128_desc(sK, KBLK, 1024), 0,
-                                           sw128_desc(sK, KBLK, 1024), 0, ID_M128N128_MM, 1);
-                    CCQ_TRACE(1, n, 8);
-                    if (n > 0 && !mbar_wait(smem_u32(&aux.eq_free), (n - 1) & 1, abort)) break;
-                    tc_fence_after();
-                    CCQ_TRACE(1, n, 5);
-                    // E^T = LA^T U^T, colsum(K)
+                                              sw128_desc(sK, KBLK, 1024), 0, ID_M128N128_MM, 1);
+                    // E^T = LA^T U^T
                     mma_k_loop<true, false, 4>(tmem + E0_COL, sw128_desc(sLA, BOX, 1024), 0,
-                                            sw128_desc(sUX, 0, 1024), 0, ID_M128N64_MK, 0);
-                    mma_k_loop<true, false, 4>(tmem + KS_COL, sw128_desc(sK, KBLK, 1024), 0,
-                                            sw128_desc(sUX + 64 * 128, 0, 1024), 0, ID_M128N16_MK, 0);
-                    mma_commit(smem_u32(&aux.eq_full));
-                    CCQ_TRACE(1, n, 9);
+                                               sw128_desc(sUX, 0, 1024), 0, ID_M128N64_MK, 0);
+                    CCQ_TRACE(1, n, 8);
                     if (!mbar_wait(smem_u32(&aux.ahat_ready), n & 1, abort)) break;
                     tc_fence_after();
                     CCQ_TRACE(1, n, 2);
                     const uint32_t sAH = smem_u32(smem + CovLayout::AH);
-                    // P^T += K^T Ah^T
+                    // P^T += K^T Ah^T; this commit covers every MMA of the chunk
                     mma_k_loop<true, false, 4>(tmem + P_COL(b), sw128_desc(sK, KBLK, 1024), 0,
-                                            sw128_desc(sAH, 0, 1024), 0, ID_M128N64_MK, 1);
+                                               sw128_desc(sAH, 0, 1024), 0, ID_M128N64_MK, 1);
                     mma_commit(smem_u32(&aux.p_full[b]));
                     CCQ_TRACE(1, n, 3);
                 }
@@ -442,6 +450,8 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                                                sw128_desc(sQT, 16384, 1024), 0, ID_M128N64_MM, 0);
                         mma_commit(smem_u32(&aux.stage1));
                         CCQ_TRACE(1, n, 7);
+                        if (!mbar_wait(smem_u32(&aux.vfull[s]), ph2, abort)) break;
+                        tc_fence_after();
                         // S = Sb + Kh^T V (Sb already in TMEM)
                         mma_k_loop<false, true, 4>(tmem + S_COL, sw128_desc(sKH, 0, 1024), 0,
                                                 sw128_desc(sV, BOX, 1024), 0, ID_M128N128_KM, 1);
@@ -511,7 +521,10 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             tc_fence_before();
             fence_async_smem();
             epi_sync_any(false);
-            if (tid == 0) mbar_arrive(smem_u32(&aux.c0_ready));
+            if (tid == 0) {
+                mbar_arrive(smem_u32(&aux.c0_ready));
+                mbar_arrive(smem_u32(&aux.m_ready));
+            }
         }
 
         for (int n = 0; n < nch; ++n) {
@@ -522,16 +535,36 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             const bool more = n + 1 < nch;
             if (tid == 0) CCQ_TRACE(0, n, 0);
 
-            // ---- gate, s_i and Ah (rows in lanes 0-15; quarter qt takes 16 columns)
-            bool ok = wait_all(smem_u32(&aux.aqk_full), n & 1, abort);
+            // ---- row sums of A (rows in lanes 0-15; quarter qt takes 16 columns) and
+            //      column sums of K (thread = channel c, quarter qt takes 16 tokens)
+            bool ok = wait_all(smem_u32(&aux.aqk_full), n & 1, abort) &&
+                      wait_all(smem_u32(&aux.full[b]), ph2, abort);
             tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 1);
             uint32_t a[16], dt[4];
+            const bool valid = r < Lc;
+            float rt = 0.f, lam = 0.f;  // 1/t_i; gate (qt == 0)
             if (ok) {
                 tmem_ld16(tl + AQK_COL + 16 * qt, a);
                 tmem_ld4(tl + AQK_COL + 64, dt);
+                // (rows past the tail were zero-filled by the tensor copy)
+                const uint8_t *sKs = smem + CovLayout::K + b * KTILE;
+                float k0 = 0.f, k1 = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; j += 2) {
+                    k0 += bf16_at(sKs, 16 * qt + j, c, 80);
+                    k1 += bf16_at(sKs, 16 * qt + j + 1, c, 80);
+                }
+                aux.kpart[qt][c] = k0 + k1;
+                rt = __fdividef(1.f, (float)(p.t0 + (long long)(c0t + r + 1)));
                 tmem_ld_wait();
                 if (tid == 0) CCQ_TRACE(0, n, 2);
+                if (qt == 0 && lane < 16 && valid) {
+                    const size_t ti = (size_t)bh * T + c0t + r;
+                    lam = p.lambda_in ? p.lambda_in[ti]
+                                      : __fdividef(1.f, 1.f + __expf(-((u2f(dt[2]) + u2f(dt[3])) + b_lam)));
+                    if (p.lambda_out) p.lambda_out[ti] = lam;
+                }
                 float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
                 for (int j = 0; j < 16; j += 2) {
@@ -542,23 +575,17 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             }
             if (epi_sync_any(!ok)) { fail = true; break; }
             if (tid == 0) CCQ_TRACE(0, n, 3);
+
+            // ---- gate, s_i, Ah; m after this chunk (dot rows of the next stage)
+            const float m_next =
+                m_cur + ((aux.kpart[0][c] + aux.kpart[1][c]) + (aux.kpart[2][c] + aux.kpart[3][c]));
             if (lane < 16) {
-                const bool valid = r < Lc;
                 const float mq = u2f(dt[0]) + u2f(dt[1]);
-                const float wq = u2f(dt[2]) + u2f(dt[3]);
-                const float rt = __fdividef(1.f, (float)(p.t0 + (long long)(c0t + r + 1)));  // 1/t_i
                 const float sdt =
                     (mq + ((aux.part[0][r] + aux.part[1][r]) + (aux.part[2][r] + aux.part[3][r]))) * rt;
-                if (qt == 0) {
-                    float lam = 0.f;
-                    if (valid) {
-                        const size_t ti = (size_t)bh * T + c0t + r;
-                        lam = p.lambda_in ? p.lambda_in[ti]
-                                          : __fdividef(1.f, 1.f + __expf(-(wq + b_lam)));
-                        if (p.lambda_out) p.lambda_out[ti] = lam;
-                    }
+                if (qt == 0)
                     aux.tok[r] = valid ? make_float2(lam * rt, sdt) : make_float2(0.f, 0.f);
-                }
+                if (tid == 0) CCQ_TRACE(2, n, 1);
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
                     float v[8];
@@ -570,59 +597,25 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     store8(smem + CovLayout::AH + sw128_chunk(r, 16 * qt + 8 * g, 64), v);
                 }
             }
-            tc_fence_before();
-            fence_async_smem();
-            if (epi_sync_any(false)) { fail = true; break; }
-            if (tid == 0) {
-                mbar_arrive(smem_u32(&aux.ahat_ready));
-                CCQ_TRACE(0, n, 4);
+            if (more && qt == 0) {  // m rows of the next chunk's K stage
+                const float mh = __bfloat162float(__float2bfloat16_rn(m_next));
+                put_bf16(smem + dot_off(b ^ 1, 0, c), mh);
+                put_bf16(smem + dot_off(b ^ 1, 1, c), m_next - mh);
             }
-
-            // ---- next chunk's operands: C0 snapshot (C accumulator after dC_n), m += colsum K_n
-            ok = wait_all(smem_u32(&aux.eq_full), n & 1, abort);
-                        tc_fence_after();
-            if (tid == 0) CCQ_TRACE(0, n, 5);
-            float m_next = m_cur;
-            if (ok) {
-                uint32_t ks[4];
-                tmem_ld4(tl + KS_COL, ks);
-                tmem_ld_wait();
-                if (tid == 0) CCQ_TRACE(0, n, 6);
-                m_next = m_cur + u2f(ks[0]);
-                if (more) {
-                    uint8_t *c0n = smem + CovLayout::C0 + (b ^ 1) * 32768;
-#pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        uint32_t cr[16];
-                        tmem_ld16(tl + C_COL + 32 * qt + 16 * hb, cr);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int g = 0; g < 2; ++g) {
-                            float v[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = u2f(cr[8 * g + e]);
-                            store8(c0n + sw128_chunk(c, 32 * qt + 16 * hb + 8 * g, 128), v);
-                        }
-                    }
-                    if (qt == 0) {  // m rows of the next chunk's K stage
-                        const float mh = __bfloat162float(__float2bfloat16_rn(m_next));
-                        put_bf16(smem + dot_off(b ^ 1, 0, c), mh);
-                        put_bf16(smem + dot_off(b ^ 1, 1, c), m_next - mh);
-                    }
-                }
-            }
+            if (tid == 0) CCQ_TRACE(2, n, 2);
             tc_fence_before();
             fence_async_smem();
             if (tid == 0) bulk_wait_read1();  // send buffer b (chunk n-2) has been read
-            if (epi_sync_any(!ok)) { fail = true; break; }
+            if (epi_sync_any(false)) { fail = true; break; }
             if (tid == 0) {
-                if (more) mbar_arrive(smem_u32(&aux.c0_ready));
-                CCQ_TRACE(0, n, 7);
+                mbar_arrive(smem_u32(&aux.ahat_ready));
+                if (more) mbar_arrive(smem_u32(&aux.m_ready));
+                CCQ_TRACE(0, n, 4);
             }
 
-            // ---- cleaned, decay-scaled query Qt^T (thread = channel c, 16 tokens)
-            ok = wait_all(smem_u32(&aux.p_full[b]), ph2, abort) &&
-                 wait_all(smem_u32(&aux.full[b]), ph2, abort);
+            // ---- cleaned, decay-scaled query Qt^T (thread = channel c, 16 tokens),
+            //      then the next chunk's C0 snapshot (C after this chunk's update)
+            ok = wait_all(smem_u32(&aux.p_full[b]), ph2, abort);
             tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 8);
             if (ok) {
@@ -649,14 +642,32 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     }
                     store8(qtb + sw128_chunk(c, i0, 128), v);
                 }
+                if (tid == 0) CCQ_TRACE(2, n, 5);
+                if (more) {
+                    uint8_t *c0n = smem + CovLayout::C0 + (b ^ 1) * 32768;
+#pragma unroll
+                    for (int hb = 0; hb < 2; ++hb) {
+                        uint32_t cr[16];
+                        tmem_ld16(tl + C_COL + 32 * qt + 16 * hb, cr);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int g = 0; g < 2; ++g) {
+                            float v[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = u2f(cr[8 * g + e]);
+                            store8(c0n + sw128_chunk(c, 32 * qt + 16 * hb + 8 * g, 128), v);
+                        }
+                    }
+                }
             }
+            if (tid == 0) CCQ_TRACE(2, n, 4);
             tc_fence_before();
             fence_async_smem();
             if (epi_sync_any(!ok)) { fail = true; break; }
             if (tid == 0) {
                 CCQ_TRACE(0, n, 10);
-                mbar_arrive(smem_u32(&aux.eq_free));
-                mbar_arrive(smem_u32(&aux.empty[b]));  // stage b: MMAs done (p_full), Q tile read
+                if (more) mbar_arrive(smem_u32(&aux.c0_ready));
+                mbar_arrive(smem_u32(&aux.empty[b]));  // stage b: MMAs done (p_full), Q, K read
                 bool sent = true;
                 if (n >= 2)
                     sent = mbar_wait(smem_u32(&aux.qt_empty[b]), ((n >> 1) - 1) & 1, abort, true);
@@ -674,7 +685,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         }
         // ---- final state: C (TMEM accumulator), m
         if (!fail && nch > 0) {
-            const bool ok = wait_all(smem_u32(&aux.eq_full), (nch - 1) & 1, abort);
+            const bool ok = wait_all(smem_u32(&aux.p_full[(nch - 1) & 1]), ((nch - 1) >> 1) & 1, abort);
             tc_fence_after();
             if (ok && p.C_out) {
                 uint32_t cr[32];
@@ -694,7 +705,8 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         // ============================================================ CTA 1 element-wise
         bool fail = false;
 
-        // Kh^T = (K * exp(E))^T of chunk k from E^T, K^T in TMEM; gamma = exp(R)
+        // Kh^T = (K * exp(E))^T of chunk k from E^T in TMEM and the K tile;
+        // gamma = exp(R), R the chunk's total log-decay per channel
         auto kh_phase = [&](int k, float &gam) -> bool {
             // E^T of chunk k > 0 was committed with chunk k-1's first MMA group
             // (stage1), which every element-wise thread has already waited for
@@ -734,10 +746,16 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             fence_async_smem();
             if (epi_sync_any(!ok)) return false;
             if (tid == 0 && k > 0) CCQ_TRACE(0, k - 1, 9);
-            if (tid == 0) mbar_arrive(smem_u32(&aux.kh_ready));
+            if (tid == 0) {
+                mbar_arrive(smem_u32(&aux.kh_ready));
+                // K read here, log alpha read by chunk k's E^T MMAs (complete:
+                // covered by ek_full or the previous chunk's stage1)
+                mbar_arrive(smem_u32(&aux.empty[k & 1]));
+            }
             return true;
         };
-        // Sb = gamma * S: rescale the S accumulator in TMEM and snapshot it (bf16)
+        // Sb = gamma * S: rescale the S accumulator in TMEM (k > 0; chunk 0
+        // starts from S0) and snapshot it as the bf16 operand
         auto sb_phase = [&](int k, float gam) -> bool {
             bool ok = true;
             uint32_t sr[32];
@@ -852,7 +870,6 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 bulk_commit();
                 CCQ_TRACE(0, n, 5);
             }
-
         }
         // ---- final state S (TMEM accumulator)
         if (!fail && nch > 0 && p.S_out) {
