@@ -2,9 +2,13 @@
 fp32 state) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gla_fwd|gdn_fwd|gla_step|gdn_step]
 
-One step = one CCQ-GLA forward over the whole batch (read + gate + stats +
-GLA write/read, final state written).  Inputs are seeded synthetic data with
+Default (the headline): one step = one CCQ-GLA forward over the whole batch
+(read + gate + stats + GLA write/read, final state written).  The other
+workloads measure the rest of the library on their own JSON line: the Gated
+DeltaNet forward (B2 H16 T8192 d128) and the single-token decode steps
+(B64 H16 d128, state resident on the device and updated in place).  Inputs are seeded synthetic data with
 the workload's distributions (anisotropic keys with one needle per sequence).
 For N > 1 (launched by torch.distributed.run) every rank runs its own replica
 of the workload on its own GPU (weak scaling, no collective on the data path);
@@ -161,7 +165,7 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def oracle_sample(inp, w, max_seconds: float = 20.0):
+def oracle_sample(inp, w, max_seconds: float = 20.0, backbone: str = "gla"):
     """Time the fp64 oracle (as it stands) on a bounded sample of the workload:
     whole sequences of a few (b, h) pairs, one pair per host thread."""
     import oracle
@@ -170,13 +174,13 @@ def oracle_sample(inp, w, max_seconds: float = 20.0):
     pairs = [(b, h) for b in range(w.B) for h in range(w.H)]
     # calibrate on one pair, then size the sample to about max_seconds
     t0 = time.perf_counter()
-    oracle.run_inputs("gla", inp, bh=pairs[:1], stop=1024, nthreads=1)
+    oracle.run_inputs(backbone, inp, bh=pairs[:1], stop=1024, nthreads=1)
     per_tok = (time.perf_counter() - t0) / 1024
     n_pairs = max(1, min(len(pairs), int(max_seconds * threads / (per_tok * w.T))))
     n_pairs = max(1, (n_pairs // threads) * threads) if n_pairs >= threads else n_pairs
     sample = pairs[:n_pairs]
     t0 = time.perf_counter()
-    oracle.run_inputs("gla", inp, bh=sample, nthreads=threads)
+    oracle.run_inputs(backbone, inp, bh=sample, nthreads=threads)
     dt = time.perf_counter() - t0
     head_tokens = len(sample) * w.T
     tokens_per_s = head_tokens / w.H / dt  # tokens of the workload (all H heads) per second
@@ -213,11 +217,19 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def gdn_flops_per_head_token(d: int, L: int = L_FLOP) -> float:
+    """Gated DeltaNet chunk-form contraction FLOPs per head-token:
+    14 L d + 10 d^2 + (2/3) L^2 (covariance read as for GLA plus the WY
+    transform, the triangular inverse and the state update)."""
+    return 14 * L * d + 10 * d * d + (2.0 / 3.0) * L * L
+
+
 def run_ours(args, world, rank, local):
     import ccq_read_side_gb300 as ccq
     from ccq_read_side_gb300.workloads import WORKLOADS, make_inputs
 
-    w = WORKLOADS[WORKLOAD_INDEX]
+    gdn = args.workload == "gdn_fwd"
+    w = WORKLOADS[4 if gdn else WORKLOAD_INDEX]
     inp = make_inputs(w)
     dev = torch.device("cuda", torch.cuda.current_device())
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
@@ -228,8 +240,12 @@ def run_ours(args, world, rank, local):
     flush = torch.empty(int(2 * l2) // 4, dtype=torch.int32, device=dev)
 
     def step():
-        ccq.gla_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["w_lambda"], d["b_lambda"], o=o,
-                    stream=stream)
+        if gdn:
+            ccq.gdn_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["w_lambda"],
+                        d["b_lambda"], o=o, stream=stream)
+        else:
+            ccq.gla_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["w_lambda"], d["b_lambda"],
+                        o=o, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -260,24 +276,28 @@ def run_ours(args, world, rank, local):
     tokens = w.B * w.T
     t_step = total / args.steps
     value = tokens * world / t_step
-    F = flops_per_head_token(w.dk)
+    F = gdn_flops_per_head_token(w.dk) if gdn else flops_per_head_token(w.dk)
     tflops = F * head_tokens / t_step / 1e12
     hbm_peak, bf16_peak, src = load_peaks()
-    alg_bytes = bytes_per_head_token(w.dk) * head_tokens
+    # GDN: q, k, v, o per channel plus the scalar log alpha and beta per token
+    alg_bytes = (4 * w.dk * 2 + 4 if gdn else bytes_per_head_token(w.dk)) * head_tokens
     achieved_gbs = alg_bytes / t_step / 1e9
 
     # ---- e2e through the public API with host buffers (pinned), copies timed
     host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    h2d = sum(host[k].numel() * host[k].element_size()
-              for k in ("q", "k", "v", "log_alpha", "w_lambda", "b_lambda"))
+    keys = ("q", "k", "v", "log_alpha", "w_lambda", "b_lambda") + (("beta",) if gdn else ())
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
     d2h = o_host.numel() * o_host.element_size()
 
     def e2e_step():
-        dd = {k: host[k].to(dev, non_blocking=True)
-              for k in ("q", "k", "v", "log_alpha", "w_lambda", "b_lambda")}
-        oo, _ = ccq.gla_fwd(dd["q"], dd["k"], dd["v"], dd["log_alpha"], dd["w_lambda"],
-                            dd["b_lambda"], want_state=False, stream=stream)
+        dd = {k: host[k].to(dev, non_blocking=True) for k in keys}
+        if gdn:
+            oo, _ = ccq.gdn_fwd(dd["q"], dd["k"], dd["v"], dd["log_alpha"], dd["beta"],
+                                dd["w_lambda"], dd["b_lambda"], want_state=False, stream=stream)
+        else:
+            oo, _ = ccq.gla_fwd(dd["q"], dd["k"], dd["v"], dd["log_alpha"], dd["w_lambda"],
+                                dd["b_lambda"], want_state=False, stream=stream)
         o_host.copy_(oo, non_blocking=True)
 
     for _ in range(max(1, min(args.warmup, 3))):
@@ -296,12 +316,13 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu, _ = oracle_sample(inp, w)
+        cpu, _ = oracle_sample(inp, w, backbone="gdn" if gdn else "gla")
 
     if rank != 0:
         return
     line = {
-        "metric": METRIC,
+        "metric": METRIC if not gdn else
+        "CCQ-GDN fwd tokens/s & TFLOP/s (frac of bf16 peak), H16 d128 T8K, 1xGB300",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -311,10 +332,12 @@ def run_ours(args, world, rank, local):
                    "parallelism": f"replicas x{world}"},
         "tflops": tflops,
         "tensor_frac": tflops / bf16_peak,
-        "flop_formula": "(8*L*d + 8*d^2) per head-token, L=64, d=128",
+        "flop_formula": ("(14*L*d + 10*d^2 + 2/3*L^2) per head-token, L=64, d=128" if gdn
+                         else "(8*L*d + 8*d^2) per head-token, L=64, d=128"),
         "head_tokens_per_s": head_tokens * world / t_step,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm_peak, "traffic": profiled_traffic(),
+                     "frac": achieved_gbs / hbm_peak,
+                     "traffic": None if gdn else profiled_traffic(),
                      "traffic_unit": "bytes per launch",
                      "peak_source": f"{src} hbm_gbs (copy)",
                      "tensor": {"achieved": tflops, "peak": bf16_peak, "unit": "TFLOP/s",
@@ -331,7 +354,152 @@ def run_ours(args, world, rank, local):
 
 
 def ccq_launches_per_step() -> int:
-    return 1  # one fused kernel launch per forward
+    return 1  # one fused kernel launch per forward (or per decode step)
+
+
+STEP_B, STEP_H, STEP_D = 64, 16, 128   # decode batch: 64 sequences x 16 heads, d 128
+
+
+def step_bytes_per_head(d: int, gdn: bool) -> int:
+    """Algorithmic HBM bytes of one decode step per head: S and C (fp32) read
+    and written, m read and written, q, k, v, o (bf16) and log alpha (bf16,
+    per channel for GLA) or log alpha and beta (one bf16 each, GDN)."""
+    state = 2 * 4 * (d * d + d * d) + 2 * 4 * d
+    vecs = 4 * d * 2 + (4 if gdn else 2 * d)
+    return state + vecs
+
+
+def run_step(args, world, rank, local):
+    """Decode: one token for each of B x H heads against a resident state."""
+    import ccq_read_side_gb300 as ccq
+    from ccq_read_side_gb300.workloads import Workload, make_inputs
+
+    gdn = args.workload == "gdn_step"
+    B, H, d = STEP_B, STEP_H, STEP_D
+    nsteps_tok = args.warmup + args.steps + 16
+    w = Workload(f"{'gdn' if gdn else 'gla'}_step_bf16_b{B}h{H}d{d}", "gdn" if gdn else "gla",
+                 "bf16", B, H, nsteps_tok, d, d, 64, 7, "iso")
+    inp = make_inputs(w)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    toks = [{k: inp[k][:, :, t].contiguous().to(dev) for k in ("q", "k", "v", "log_alpha", "beta")
+             if inp.get(k) is not None} for t in range(nsteps_tok)]
+    wl, bl = inp["w_lambda"].to(dev), inp["b_lambda"].to(dev)
+    g = torch.Generator().manual_seed(3)
+    S = (torch.randn((B, H, d, d), generator=g) * 0.1).to(dev)
+    K0 = torch.nn.functional.normalize(torch.randn((B, H, 32, d), generator=g), dim=-1)
+    C = torch.einsum("bhti,bhtj->bhij", K0, K0).contiguous().to(dev)
+    m = K0.sum(2).contiguous().to(dev)
+    o = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    prop = torch.cuda.get_device_properties(dev)
+    l2 = getattr(prop, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
+    flush = torch.empty(int(2 * l2) // 4, dtype=torch.int32, device=dev)
+    t_seen = [4096]
+
+    def step(tok):
+        if gdn:
+            ccq.gdn_step(tok["q"], tok["k"], tok["v"], tok["log_alpha"], tok["beta"], S, C, m,
+                         t_seen[0], wl, bl, o=o, stream=stream)
+        else:
+            ccq.gla_step(tok["q"], tok["k"], tok["v"], tok["log_alpha"], S, C, m, t_seen[0], wl,
+                         bl, o=o, stream=stream)
+        t_seen[0] += 1
+
+    for i in range(args.warmup):
+        step(toks[i])
+    torch.cuda.synchronize()
+    if ccq.last_device_status() != 0:
+        raise RuntimeError("device status after warm-up")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            flush.zero_()                       # the state (269 MB) is larger than L2 anyway
+            ev[i][0].record(stream)
+            step(toks[args.warmup + i])
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    times = [a.elapsed_time(b) * 1e-3 for a, b in ev]
+    total = max_over_ranks(sum(times), world)
+    if ccq.last_device_status() != 0:
+        raise RuntimeError("device status after timing")
+    t_step = total / args.steps
+    hbm_peak, _, src = load_peaks()
+    alg = step_bytes_per_head(d, gdn) * B * H
+    achieved = alg / t_step / 1e9
+
+    # e2e: the token's inputs come from pinned host memory, o goes back; the
+    # state stays resident on the device (the decode setting)
+    keys = ("q", "k", "v", "log_alpha") + (("beta",) if gdn else ())
+    host = [{k: toks[i][k].cpu().pin_memory() for k in keys} for i in range(8)]
+    o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in keys)
+    d2h = o_host.numel() * o_host.element_size()
+
+    def e2e_step(i):
+        tok = {k: host[i % 8][k].to(dev, non_blocking=True) for k in keys}
+        step(tok)
+        o_host.copy_(o, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n_e2e = 10
+    e0.record(stream)
+    for i in range(n_e2e):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / n_e2e, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        S0, C0, m0 = (x.cpu().numpy() for x in (S, C, m))
+        heads = min(B, 8)
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 5.0:
+            oracle.run(w.backbone, inp["q"][:heads, :, :1], inp["k"][:heads, :, :1],
+                       inp["v"][:heads, :, :1], inp["log_alpha"][:heads, :, :1], inp["w_lambda"],
+                       inp["b_lambda"],
+                       beta=None if inp.get("beta") is None else inp["beta"][:heads, :, :1],
+                       S0=S0[:heads], C0=C0[:heads], m0=m0[:heads], t0=t_seen[0])
+            reps += 1
+        dt = (time.perf_counter() - t0) / reps
+        cpu = {"value": heads / dt, "unit": "sequence-steps/s", "cores": oracle.default_threads(),
+               "kind": "oracle",
+               "sample": f"one step of {heads} of {B} sequences x {H} heads from a d{d} state, "
+                         f"fp64, {reps} repetitions"}
+    if rank != 0:
+        return
+    line = {
+        "metric": f"CCQ-{'GDN' if gdn else 'GLA'} decode step: sequences/s (one token each), "
+                  f"B{B} H{H} d{d}, 1xGB300",
+        "value": B * world / t_step, "unit": "sequence-steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "H": H, "dk": d, "dv": d, "inputs": "bf16",
+                   "state": "fp32, resident, updated in place",
+                   "l2": "flushed (2x L2 memset) before every timed step; state 269 MB > L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "bytes_per_step": alg, "peak_source": f"{src} hbm_gbs (copy)"},
+        "e2e": {"value": B * world / e2e_t, "unit": "sequence-steps/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
 
 
 def main():
@@ -341,6 +509,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["gla_fwd", "gdn_fwd", "gla_step", "gdn_step"],
+                    default="gla_fwd")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -348,6 +518,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.workload.endswith("_step"):
+            run_step(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

@@ -16,7 +16,7 @@ from typing import Dict, Optional, Tuple
 
 import torch
 
-__all__ = ["gla_fwd", "gdn_fwd", "last_device_status", "status_string", "CcqError",
+__all__ = ["gla_fwd", "gdn_fwd", "gla_step", "gdn_step", "last_device_status", "status_string", "CcqError",
            "library", "FLAG_L2NORM_QK", "FLAG_FP32_PATH", "FLAG_TEST_STALL", "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -53,6 +53,11 @@ def library() -> ctypes.CDLL:
     lib.ccq_gla_fwd.argtypes = [P, P, P, P, P, P, P, P, P] + common_tail
     lib.ccq_gdn_fwd.restype = I
     lib.ccq_gdn_fwd.argtypes = [P, P, P, P, P, P, P, P, P, P] + common_tail
+    step_tail = [P, P, P, P, P, P, ctypes.c_int64, I, I, I, I, I, ctypes.c_uint, P]
+    lib.ccq_gla_step.restype = I
+    lib.ccq_gla_step.argtypes = [P, P, P, P, P, P] + step_tail
+    lib.ccq_gdn_step.restype = I
+    lib.ccq_gdn_step.argtypes = [P, P, P, P, P, P, P] + step_tail
     lib.ccq_status_string.restype = ctypes.c_char_p
     lib.ccq_status_string.argtypes = [I]
     lib.ccq_last_device_status.restype = I
@@ -161,3 +166,58 @@ def gdn_fwd(q, k, v, log_alpha, beta, w_lambda=None, b_lambda=None, *, lambda_in
     """CCQ forward on the Gated DeltaNet backbone (scalar log_alpha and beta [B,H,T])."""
     return _fwd("gdn", q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in, S0, C0, m0, t0,
                 o, lambda_out, want_state, chunk, flags, stream)
+
+
+def _step(backbone, q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in, S, C, m, t0, o,
+          lambda_out, flags, stream):
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    dev = q.device
+    for name, t, shp in (("q", q, (B, H, dk)), ("k", k, (B, H, dk)), ("v", v, (B, H, dv)),
+                         ("log_alpha", log_alpha, (B, H, dk) if backbone == "gla" else (B, H))):
+        _need(t, name, dt, shp, dev)
+    if backbone == "gdn":
+        _need(beta, "beta", dt, (B, H), dev)
+    _need(w_lambda, "w_lambda", torch.float32, (H, dk), dev)
+    _need(b_lambda, "b_lambda", torch.float32, (H,), dev)
+    _need(lambda_in, "lambda_in", torch.float32, (B, H), dev)
+    _need(S, "S", torch.float32, (B, H, dk, dv), dev)
+    _need(C, "C", torch.float32, (B, H, dk, dk), dev)
+    _need(m, "m", torch.float32, (B, H, dk), dev)
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=dt, device=dev)
+    _need(o, "o", dt, (B, H, dv), dev)
+    _need(lambda_out, "lambda_out", torch.float32, (B, H), dev)
+    lib = library()
+    tail = (_ptr(o), _ptr(S), _ptr(C), _ptr(m), int(t0), B, H, dk, dv, _DTYPES[dt], int(flags),
+            _stream(stream))
+    with torch.cuda.device(dev):
+        if backbone == "gla":
+            rc = lib.ccq_gla_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(w_lambda),
+                                  _ptr(b_lambda), _ptr(lambda_in), _ptr(lambda_out), *tail)
+        else:
+            rc = lib.ccq_gdn_step(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                                  _ptr(w_lambda), _ptr(b_lambda), _ptr(lambda_in),
+                                  _ptr(lambda_out), *tail)
+    if rc != 0:
+        raise CcqError(rc, f"ccq_{backbone}_step")
+    return o
+
+
+def gla_step(q, k, v, log_alpha, S, C, m, t0: int, w_lambda=None, b_lambda=None, *,
+             lambda_in=None, o=None, lambda_out=None, flags: int = 0, stream=None):
+    """One decode step on the GLA backbone: q, k, log_alpha [B,H,dk], v [B,H,dv].
+    S, C, m (fp32) hold the state after t0 tokens and are updated in place to
+    the state after this token.  Returns o [B,H,dv]."""
+    return _step("gla", q, k, v, log_alpha, None, w_lambda, b_lambda, lambda_in, S, C, m, t0,
+                 o, lambda_out, flags, stream)
+
+
+def gdn_step(q, k, v, log_alpha, beta, S, C, m, t0: int, w_lambda=None, b_lambda=None, *,
+             lambda_in=None, o=None, lambda_out=None, flags: int = 0, stream=None):
+    """One decode step on the Gated DeltaNet backbone (log_alpha, beta [B,H])."""
+    return _step("gdn", q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in, S, C, m, t0,
+                 o, lambda_out, flags, stream)

@@ -28,6 +28,12 @@ cudaError_t launch_simt(const CcqParams &p, bool gdn, bool bf16, cudaStream_t st
 // shape is not one it takes.
 cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st);
 bool tc_gla_supported(const CcqParams &p);
+// Single-token step (step.cu).
+cudaError_t launch_step(const void *q, const void *k, const void *v, const void *log_alpha,
+                        const void *beta, const float *w_lambda, const float *b_lambda,
+                        const float *lambda_in, float *lambda_out, void *o, float *S, float *C,
+                        float *m, long long t0, int B, int H, int dk, int dv, bool gdn, bool bf16,
+                        unsigned flags, unsigned int *status, cudaStream_t st);
 
 static ccq_status check_common(const CcqParams &p, ccq_dtype dtype) {
     if (p.B < 0 || p.H < 0 || p.T < 0 || p.chunk < 0 || p.t0 < 0) return CCQ_ERR_INVALID_ARG;
@@ -44,6 +50,25 @@ static ccq_status check_common(const CcqParams &p, ccq_dtype dtype) {
         return CCQ_ERR_INVALID_ARG;
     if ((long long)p.B * p.H > 0x7fffffffLL) return CCQ_ERR_UNSUPPORTED;
     if ((long long)p.T + p.t0 > (1LL << 40)) return CCQ_ERR_UNSUPPORTED;
+    return CCQ_OK;
+}
+
+static ccq_status check_step(const void *q, const void *k, const void *v,
+                             const void *log_alpha, const float *w_lambda,
+                             const float *b_lambda, const float *lambda_in, const void *o,
+                             const float *S, const float *C, const float *m, int64_t t0, int B,
+                             int H, int dk, int dv, ccq_dtype dtype, unsigned flags) {
+    if (B < 0 || H < 0 || t0 < 0) return CCQ_ERR_INVALID_ARG;
+    if (dtype != CCQ_DTYPE_F32 && dtype != CCQ_DTYPE_BF16) return CCQ_ERR_UNSUPPORTED;
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return CCQ_ERR_UNSUPPORTED;
+    if (flags & ~CCQ_FLAG_L2NORM_QK) return CCQ_ERR_INVALID_ARG;
+    if ((long long)B * H * 8 > 0x7fffffffLL) return CCQ_ERR_UNSUPPORTED;
+    if (t0 >= (1LL << 40)) return CCQ_ERR_UNSUPPORTED;
+    if ((long long)B * H == 0) return CCQ_OK;
+    if (!q || !k || !v || !log_alpha || !o || !S || !C || !m) return CCQ_ERR_INVALID_ARG;
+    if (!lambda_in && (!w_lambda || !b_lambda)) return CCQ_ERR_INVALID_ARG;
+    // the state rows are moved as float4
+    if (((uintptr_t)S & 15u) || ((uintptr_t)C & 15u)) return CCQ_ERR_INVALID_ARG;
     return CCQ_OK;
 }
 
@@ -99,6 +124,41 @@ extern "C" ccq_status ccq_gdn_fwd(const void *q, const void *k, const void *v,
     if (!p.status) return CCQ_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     return to_status(launch_simt(p, true, dtype == CCQ_DTYPE_BF16, st));
+}
+
+extern "C" ccq_status ccq_gla_step(const void *q, const void *k, const void *v,
+                                   const void *log_alpha, const float *w_lambda,
+                                   const float *b_lambda, const float *lambda_in,
+                                   float *lambda_out, void *o, float *S, float *C, float *m,
+                                   int64_t t0, int B, int H, int dk, int dv, ccq_dtype dtype,
+                                   unsigned flags, ccq_stream_t stream) {
+    ccq_status s = check_step(q, k, v, log_alpha, w_lambda, b_lambda, lambda_in, o, S, C, m, t0,
+                              B, H, dk, dv, dtype, flags);
+    if (s != CCQ_OK) return s;
+    unsigned int *st_word = status_word();
+    if (!st_word) return CCQ_ERR_CUDA;
+    return to_status(launch_step(q, k, v, log_alpha, nullptr, w_lambda, b_lambda, lambda_in,
+                                 lambda_out, o, S, C, m, (long long)t0, B, H, dk, dv, false,
+                                 dtype == CCQ_DTYPE_BF16, flags, st_word,
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" ccq_status ccq_gdn_step(const void *q, const void *k, const void *v,
+                                   const void *log_alpha, const void *beta,
+                                   const float *w_lambda, const float *b_lambda,
+                                   const float *lambda_in, float *lambda_out, void *o, float *S,
+                                   float *C, float *m, int64_t t0, int B, int H, int dk, int dv,
+                                   ccq_dtype dtype, unsigned flags, ccq_stream_t stream) {
+    ccq_status s = check_step(q, k, v, log_alpha, w_lambda, b_lambda, lambda_in, o, S, C, m, t0,
+                              B, H, dk, dv, dtype, flags);
+    if (s != CCQ_OK) return s;
+    if (!beta && (long long)B * H > 0) return CCQ_ERR_INVALID_ARG;
+    unsigned int *st_word = status_word();
+    if (!st_word) return CCQ_ERR_CUDA;
+    return to_status(launch_step(q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in,
+                                 lambda_out, o, S, C, m, (long long)t0, B, H, dk, dv, true,
+                                 dtype == CCQ_DTYPE_BF16, flags, st_word,
+                                 reinterpret_cast<cudaStream_t>(stream)));
 }
 
 extern "C" const char *ccq_status_string(ccq_status s) {

@@ -1,0 +1,289 @@
+// step.cu -- single-token CCQ step (decode): one new token per (b, h) against
+// a carried state S, C, m with t0 tokens already seen, updated in place.
+//
+// The token's read is the same operator as the chunked forward (10100.com
+// article, "method", item 1; gist.science summary of 2606.01294, section 2,
+// "mechanism" and "integration"):
+//   write  GLA  S <- Diag(alpha) S + k v^T
+//          GDN  S <- alpha (S - beta k (k^T S)) + beta k v^T
+//          C <- C + k k^T,  m <- m + k,  n = t0 + 1
+//   read   lambda = sigmoid(w . q + b)  (or the given lambda)
+//          q_clean = q - lambda (C q / n - mu (mu . q)),  mu = m / n
+//          o = S^T q_clean
+// A step streams the whole state of every head once in and once out, so it
+// is bound by HBM bandwidth: the kernel's job is to move 2 x 4 (dk dv + dk dk)
+// bytes per head at full speed.
+//
+// Layout of the work: one cluster of NC = 4 CTAs per (b, h); CTA r owns rows
+// [r R, (r+1) R) of S and of C (R = dk / 4), moved in and out by bulk
+// asynchronous copies.  Everything row-local (the row
+// updates, (C q)_c and so q_clean_c) stays in the CTA; the two sums over all
+// rows -- k^T S (GDN, before the update) and S^T q_clean -- are reduced
+// across the cluster through distributed shared memory.  The small vector
+// work (norms, gate, mu . q) is repeated by every CTA instead of exchanged.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "sm103.cuh"
+
+namespace ccq {
+namespace step {
+
+#ifndef CCQ_STEP_NC
+#define CCQ_STEP_NC 4
+#endif
+#ifndef CCQ_STEP_THREADS
+#define CCQ_STEP_THREADS 256
+#endif
+constexpr int NC = CCQ_STEP_NC;  // CTAs per (b, h)
+constexpr int NTHREADS = CCQ_STEP_THREADS;
+
+struct StepParams {
+    const void *q, *k, *v, *log_alpha, *beta;
+    const float *w_lambda, *b_lambda, *lambda_in;
+    float *lambda_out;
+    void *o;
+    float *S, *C, *m;
+    long long t0;
+    int BH, H;
+    unsigned flags;
+    unsigned int *status;
+};
+
+template <typename T>
+__device__ __forceinline__ float ld1(const T *p, size_t i) {
+    return io<T>::load(p + i);
+}
+
+__device__ __forceinline__ float block_sum(float x, float *red) {
+    x = warp_sum(x);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();  // red may still be read by a previous reduction
+    if (lane == 0) red[warp] = x;
+    __syncthreads();
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < NTHREADS / 32; ++w) s += red[w];
+    return s;
+}
+
+// Sum over the cluster of a DV-vector held in every CTA's shared memory at
+// the same offset (`part`); CTA `rank` reduces elements [rank*DV/NC, ...) and
+// hands each to `sink(j, value)`.
+template <int DV, typename Sink>
+__device__ __forceinline__ void cluster_reduce(const float *part, uint32_t rank, Sink sink) {
+    constexpr int PER = DV / NC;
+    const int tid = threadIdx.x;
+    if (tid < PER) {
+        const int j = (int)rank * PER + tid;
+        const uint32_t local = sm103::smem_u32(part + j);
+        float s = 0.f;
+#pragma unroll
+        for (uint32_t r = 0; r < NC; ++r) {
+            float x;
+            asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                         : "=f"(x)
+                         : "r"(sm103::mapa(local, r))
+                         : "memory");
+            s += x;
+        }
+        sink(j, s);
+    }
+}
+
+template <bool GDN, typename TIn, int DK, int DV>
+__global__ void __cluster_dims__(NC, 1, 1) __launch_bounds__(NTHREADS)
+ccq_step_kernel(const __grid_constant__ StepParams p) {
+    constexpr int R = DK / NC;  // rows of S and C in this CTA
+    __shared__ __align__(16) float sS[R][DV];
+    __shared__ __align__(16) float sC[R][DK];
+    __shared__ float qv[DK], kv[DK], mv[DK], av[DK];
+    __shared__ float vv[DV], upart[DV], u[DV], opart[DV];
+    __shared__ float qc[R];
+    __shared__ float red[NTHREADS / 32];
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+
+    const int tid = threadIdx.x;
+    const uint32_t rank = sm103::cluster_ctarank();
+    const int bh = blockIdx.x / NC, h = bh % p.H;
+    const int r0 = (int)rank * R;
+    const TIn *q = static_cast<const TIn *>(p.q) + (size_t)bh * DK;
+    const TIn *k = static_cast<const TIn *>(p.k) + (size_t)bh * DK;
+    const TIn *v = static_cast<const TIn *>(p.v) + (size_t)bh * DV;
+    float *S = p.S + ((size_t)bh * DK + r0) * DV;
+    float *C = p.C + ((size_t)bh * DK + r0) * DK;
+    float *m = p.m + (size_t)bh * DK;
+
+    // ---- state rows in flight first (they are the bandwidth): two bulk copies
+    constexpr uint32_t SBYTES = R * DV * 4, CBYTES = R * DK * 4;
+    if (tid == 0) {
+        abort_flag = 0;
+        sm103::mbar_init(sm103::smem_u32(&bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        sm103::mbar_expect_tx(sm103::smem_u32(&bar), SBYTES + CBYTES);
+        sm103::bulk_load(sm103::smem_u32(&sS[0][0]), S, SBYTES, sm103::smem_u32(&bar));
+        sm103::bulk_load(sm103::smem_u32(&sC[0][0]), C, CBYTES, sm103::smem_u32(&bar));
+    }
+    for (int i = tid; i < DK; i += NTHREADS) {
+        qv[i] = ld1(q, i);
+        kv[i] = ld1(k, i);
+        mv[i] = m[i];
+        if (!GDN) av[i] = ld1(static_cast<const TIn *>(p.log_alpha), (size_t)bh * DK + i);
+    }
+    for (int i = tid; i < DV; i += NTHREADS) vv[i] = ld1(v, i);
+    __syncthreads();  // barrier initialised, vectors in place
+    // bounded wait for the state rows; a wait that gives up records the error
+    // and the CTA carries on (garbage in, but every cluster barrier is reached)
+    if (!sm103::mbar_wait(sm103::smem_u32(&bar), 0, &abort_flag) && tid == 0)
+        record_status(p.status, CCQ_ERR_TIMEOUT);
+
+    // ---- optional L2 normalisation of q and k (every CTA, from the full vectors)
+    if (p.flags & CCQ_FLAG_L2NORM_QK) {
+        float sq = 0.f, sk = 0.f;
+        for (int i = tid; i < DK; i += NTHREADS) {
+            sq += qv[i] * qv[i];
+            sk += kv[i] * kv[i];
+        }
+        const float nq = rsqrtf(block_sum(sq, red) + 1e-6f);
+        const float nk = rsqrtf(block_sum(sk, red) + 1e-6f);
+        __syncthreads();
+        for (int i = tid; i < DK; i += NTHREADS) {
+            qv[i] *= nq;
+            kv[i] *= nk;
+        }
+        __syncthreads();
+    }
+
+    // ---- gate and mu . q (m after this token's key)
+    const double n = (double)(p.t0 + 1);
+    const float rn = (float)(1.0 / n);
+    float dw = 0.f, dm = 0.f;
+    for (int i = tid; i < DK; i += NTHREADS) {
+        if (!p.lambda_in) dw += p.w_lambda[(size_t)h * DK + i] * qv[i];
+        dm += (mv[i] + kv[i]) * qv[i];
+    }
+    const float wq = p.lambda_in ? 0.f : block_sum(dw, red);
+    const float mq = block_sum(dm, red);  // (m_new . q)
+    const float lam =
+        p.lambda_in ? p.lambda_in[bh] : 1.f / (1.f + expf(-(wq + p.b_lambda[h])));
+    const float muq = mq * rn;  // mu . q
+
+    // ---- GDN: u = k^T S over all rows, before the write
+    float alpha_s = 1.f, beta_s = 0.f;
+    if (GDN) {
+        alpha_s = expf(ld1(static_cast<const TIn *>(p.log_alpha), (size_t)bh));
+        beta_s = ld1(static_cast<const TIn *>(p.beta), (size_t)bh);
+        for (int j = tid; j < DV; j += NTHREADS) {
+            float s = 0.f;
+#pragma unroll
+            for (int c = 0; c < R; ++c) s += kv[r0 + c] * sS[c][j];
+            upart[j] = s;
+        }
+        sm103::cluster_sync();
+        cluster_reduce<DV>(upart, rank, [&](int j, float s) { u[j] = s; });
+        sm103::cluster_sync();
+        // every CTA needs all of u: gather the slices the other CTAs reduced
+        for (int j = tid; j < DV; j += NTHREADS) {
+            const uint32_t owner = (uint32_t)(j / (DV / NC));
+            float x;
+            asm volatile("ld.shared::cluster.f32 %0, [%1];"
+                         : "=f"(x)
+                         : "r"(sm103::mapa(sm103::smem_u32(&u[j]), owner))
+                         : "memory");
+            upart[j] = x;  // upart is free again: reuse it as the full u
+        }
+        __syncthreads();
+    }
+
+    // ---- row updates of S and C
+    for (int i = tid; i < R * DV; i += NTHREADS) {
+        const int c = i / DV, j = i % DV;
+        const float kc = kv[r0 + c];
+        float s = sS[c][j];
+        if (GDN)
+            s = alpha_s * (s - beta_s * kc * upart[j]) + beta_s * kc * vv[j];
+        else
+            s = expf(av[r0 + c]) * s + kc * vv[j];
+        sS[c][j] = s;
+    }
+    for (int i = tid; i < R * DK; i += NTHREADS) {
+        const int c = i / DK, j = i % DK;
+        sC[c][j] += kv[r0 + c] * kv[j];
+    }
+    // the rows are final: write them back while the read proceeds
+    sm103::fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        sm103::bulk_store(S, sm103::smem_u32(&sS[0][0]), SBYTES);
+        sm103::bulk_store(C, sm103::smem_u32(&sC[0][0]), CBYTES);
+        sm103::bulk_commit();
+    }
+
+    // ---- q_clean for this CTA's channels: (C q)_c per row, one warp per row
+    {
+        const int warp = tid >> 5, lane = tid & 31;
+        for (int c = warp; c < R; c += NTHREADS / 32) {
+            float s = 0.f;
+            for (int j = lane; j < DK; j += 32) s += sC[c][j] * qv[j];
+            s = warp_sum(s);
+            if (lane == 0) {
+                const float mu_c = (mv[r0 + c] + kv[r0 + c]) * rn;
+                qc[c] = qv[r0 + c] - lam * (s * rn - mu_c * muq);
+            }
+        }
+    }
+    __syncthreads();
+
+    // ---- partial read o = S^T q_clean over this CTA's rows, then the cluster sum
+    for (int j = tid; j < DV; j += NTHREADS) {
+        float s = 0.f;
+#pragma unroll
+        for (int c = 0; c < R; ++c) s += qc[c] * sS[c][j];
+        opart[j] = s;
+    }
+    sm103::cluster_sync();
+    TIn *o = static_cast<TIn *>(p.o) + (size_t)bh * DV;
+    cluster_reduce<DV>(opart, rank, [&](int j, float s) { io<TIn>::store(o + j, s); });
+
+    for (int c = tid; c < R; c += NTHREADS) m[r0 + c] = mv[r0 + c] + kv[r0 + c];
+    if (rank == 0 && tid == 0 && p.lambda_out) p.lambda_out[bh] = lam;
+    if (tid == 0) sm103::bulk_wait_read0();  // the state rows have left shared memory
+    sm103::cluster_sync();  // peers may still be reading this CTA's opart
+}
+
+template <bool GDN, typename TIn>
+static cudaError_t launch_t(const StepParams &p, int dk, int dv, cudaStream_t st) {
+    const dim3 grid((unsigned)(p.BH * NC)), block(NTHREADS);
+#define CCQ_STEP_CASE(DK_, DV_)                                                   \
+    if (dk == DK_ && dv == DV_) {                                                 \
+        ccq_step_kernel<GDN, TIn, DK_, DV_><<<grid, block, 0, st>>>(p);           \
+        return cudaGetLastError();                                                \
+    }
+    CCQ_STEP_CASE(64, 64)
+    CCQ_STEP_CASE(64, 128)
+    CCQ_STEP_CASE(128, 64)
+    CCQ_STEP_CASE(128, 128)
+#undef CCQ_STEP_CASE
+    return cudaErrorNotSupported;
+}
+
+}  // namespace step
+
+cudaError_t launch_step(const void *q, const void *k, const void *v, const void *log_alpha,
+                        const void *beta, const float *w_lambda, const float *b_lambda,
+                        const float *lambda_in, float *lambda_out, void *o, float *S, float *C,
+                        float *m, long long t0, int B, int H, int dk, int dv, bool gdn, bool bf16,
+                        unsigned flags, unsigned int *status, cudaStream_t st) {
+    step::StepParams p{q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in, lambda_out,
+                       o, S, C, m, t0, B * H, H, flags, status};
+    if (p.BH == 0) return cudaSuccess;
+    if (gdn) {
+        return bf16 ? step::launch_t<true, __nv_bfloat16>(p, dk, dv, st)
+                    : step::launch_t<true, float>(p, dk, dv, st);
+    }
+    return bf16 ? step::launch_t<false, __nv_bfloat16>(p, dk, dv, st)
+                : step::launch_t<false, float>(p, dk, dv, st);
+}
+
+}  // namespace ccq

@@ -116,6 +116,37 @@ ccq_status ccq_gdn_fwd(const void *q, const void *k, const void *v, const void *
                        float *C_out, float *m_out, int B, int H, int T, int dk, int dv,
                        int chunk, ccq_dtype dtype, unsigned flags, ccq_stream_t stream);
 
+/*
+ * Single-token step (decode) on the GLA backbone: one new token per (b, h)
+ * read against a carried state, which is updated in place.  Same operator as
+ * ccq_gla_fwd with T = 1 (the read uses the state after this token's write);
+ * the state is required (pass zeros and t0 = 0 for a first token).
+ *   q, k        [B, H, dk]        v, o   [B, H, dv]      (input dtype)
+ *   log_alpha   [B, H, dk]        (input dtype)
+ *   w_lambda    float32 [H, dk];  b_lambda float32 [H]   (unless lambda_in)
+ *   lambda_in, lambda_out  float32 [B, H] or NULL
+ *   S [B, H, dk, dv], C [B, H, dk, dk], m [B, H, dk]  float32, read and
+ *               overwritten with the state after the token; S and C 16-byte
+ *               aligned.  t0 = tokens the state has seen before this one.
+ * Flags: CCQ_FLAG_L2NORM_QK only.  A step moves every head's whole state once
+ * in and once out (bandwidth-bound).  Returns as ccq_gla_fwd.
+ */
+ccq_status ccq_gla_step(const void *q, const void *k, const void *v, const void *log_alpha,
+                        const float *w_lambda, const float *b_lambda, const float *lambda_in,
+                        float *lambda_out, void *o, float *S, float *C, float *m, int64_t t0,
+                        int B, int H, int dk, int dv, ccq_dtype dtype, unsigned flags,
+                        ccq_stream_t stream);
+
+/*
+ * Single-token step on the Gated DeltaNet backbone: log_alpha and beta are
+ * [B, H] (input dtype); everything else as ccq_gla_step.
+ */
+ccq_status ccq_gdn_step(const void *q, const void *k, const void *v, const void *log_alpha,
+                        const void *beta, const float *w_lambda, const float *b_lambda,
+                        const float *lambda_in, float *lambda_out, void *o, float *S, float *C,
+                        float *m, int64_t t0, int B, int H, int dk, int dv, ccq_dtype dtype,
+                        unsigned flags, ccq_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char *ccq_status_string(ccq_status s);
 

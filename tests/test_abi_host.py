@@ -31,7 +31,8 @@ def _declared():
 
 def test_header_declares_the_entry_points():
     d = _declared()
-    for n in ("ccq_gla_fwd", "ccq_gdn_fwd", "ccq_status_string", "ccq_last_device_status"):
+    for n in ("ccq_gla_fwd", "ccq_gdn_fwd", "ccq_gla_step", "ccq_gdn_step", "ccq_status_string",
+              "ccq_last_device_status"):
         assert n in d
 
 
@@ -99,3 +100,33 @@ def test_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 1, 4, 64)
     with pytest.raises(ValueError):
         ccq.gla_fwd(q, q, q, q, torch.zeros(1, 64), torch.zeros(1))
+
+
+def _step(lib, fn="ccq_gla_step", **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, la=FAKE, beta=FAKE, w=FAKE, b=FAKE, lin=None, lout=None,
+             o=FAKE, S=FAKE, C=FAKE, m=FAKE, t0=0, B=1, H=1, dk=64, dv=64, dtype=0, flags=0)
+    a.update(kw)
+    head = [a["q"], a["k"], a["v"], a["la"]] + ([a["beta"]] if fn == "ccq_gdn_step" else [])
+    return getattr(lib, fn)(*head, a["w"], a["b"], a["lin"], a["lout"], a["o"], a["S"], a["C"],
+                            a["m"], a["t0"], a["B"], a["H"], a["dk"], a["dv"], a["dtype"],
+                            a["flags"], None)
+
+
+@pytest.mark.parametrize("case,code", [
+    (dict(S=None), 1), (dict(C=None), 1), (dict(m=None), 1), (dict(q=None), 1),
+    (dict(o=None), 1), (dict(w=None), 1), (dict(t0=-1), 1), (dict(B=-1), 1),
+    (dict(S=ctypes.c_void_p(0x1004)), 1), (dict(flags=ccq.FLAG_FP32_PATH), 1),
+    (dict(dk=96), 2), (dict(dv=32), 2), (dict(dtype=5), 2),
+])
+def test_step_bad_arguments_rejected_synchronously(lib, case, code):
+    assert _step(lib, **case) == code
+    assert _step(lib, fn="ccq_gdn_step", **case) == code
+
+
+def test_gdn_step_requires_beta(lib):
+    assert _step(lib, fn="ccq_gdn_step", beta=None) == 1
+
+
+def test_step_empty_batch_needs_no_pointers(lib):
+    none = dict(q=None, k=None, v=None, la=None, o=None, S=None, C=None, m=None, w=None, b=None)
+    assert _step(lib, B=0, **none) == 0

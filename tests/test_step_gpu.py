@@ -1,0 +1,158 @@
+"""GPU parity of the single-token step (decode) against the fp64 oracle.
+
+The step is the forward with T = 1 against a carried state, so the oracle is
+the same token-by-token recurrence run for one token from that state.  The
+state S, C, m is fp32 on both sides of the boundary and is checked at the
+fp32 tolerance; o is checked at the input dtype's tolerance.
+"""
+import numpy as np
+import pytest
+import torch
+
+import ccq_read_side_gb300 as ccq
+import oracle
+from ccq_read_side_gb300.workloads import Workload, make_inputs
+from parity import check, np64
+
+pytestmark = pytest.mark.gpu
+
+def _state(rng, B, H, dk, dv, P):
+    """A plausible carried state after P unit-norm keys: C = K^T K, m = sum K."""
+    K0 = rng.standard_normal((B, H, P, dk))
+    K0 /= np.linalg.norm(K0, axis=-1, keepdims=True)
+    C0 = np.einsum("bhti,bhtj->bhij", K0, K0).astype(np.float32)
+    m0 = K0.sum(2).astype(np.float32)
+    S0 = (rng.standard_normal((B, H, dk, dv)) * 0.3).astype(np.float32)
+    return S0, C0, m0
+
+
+def _token(inp, t):
+    """Token t of every (b, h) as the step's [B, H, ...] tensors (CPU)."""
+    out = {}
+    for key in ("q", "k", "v", "log_alpha", "beta"):
+        if inp.get(key) is not None:
+            out[key] = inp[key][:, :, t].contiguous()
+    return out
+
+
+def _step(backbone, tok, S, C, m, t0, w, b, **kw):
+    d = {k: v.cuda() for k, v in tok.items()}
+    if backbone == "gla":
+        return ccq.gla_step(d["q"], d["k"], d["v"], d["log_alpha"], S, C, m, t0, w, b, **kw)
+    return ccq.gdn_step(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], S, C, m, t0, w, b,
+                        **kw)
+
+
+def _oracle_one(backbone, inp, t, S0, C0, m0, t0, **kw):
+    sl = slice(t, t + 1)
+    return oracle.run(backbone, inp["q"][:, :, sl], inp["k"][:, :, sl], inp["v"][:, :, sl],
+                      inp["log_alpha"][:, :, sl], inp["w_lambda"], inp["b_lambda"],
+                      beta=None if inp.get("beta") is None else inp["beta"][:, :, sl],
+                      S0=S0, C0=C0, m0=m0, t0=t0, **kw)
+
+
+@pytest.mark.parametrize("backbone", ["gla", "gdn"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(64, 64), (64, 128), (128, 64), (128, 128)])
+def test_step_from_carried_state(backbone, dtype, dk, dv):
+    B, H = 2, 3
+    w = Workload("step", backbone, dtype, B, H, 1, dk, dv, 64, 21 + dk + dv, "iso")
+    inp = make_inputs(w)
+    rng = np.random.default_rng(dk * 7 + dv)
+    S0, C0, m0 = _state(rng, B, H, dk, dv, 37)
+    S, C, m = (torch.from_numpy(x).cuda() for x in (S0, C0, m0))
+    lam = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    o = _step(backbone, _token(inp, 0), S, C, m, 37, inp["w_lambda"].cuda(),
+              inp["b_lambda"].cuda(), lambda_out=lam)
+    torch.cuda.synchronize()
+    assert ccq.last_device_status() == 0
+    ref = _oracle_one(backbone, inp, 0, S0, C0, m0, 37)
+    check(np64(o), ref["o"][:, :, 0], dtype, "step o")
+    np.testing.assert_allclose(np64(lam), ref["lambda"][:, :, 0], rtol=1e-5, atol=1e-6)
+    for key, got in (("S", S), ("C", C), ("m", m)):
+        check(np64(got), ref[key], "f32", "step " + key, per_head=False)
+
+
+@pytest.mark.parametrize("backbone", ["gla", "gdn"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chained_steps_match_the_sequence(backbone, dtype):
+    """T steps from the zero state (t0 = 0, 1, ...) reproduce the oracle's
+    forward over the T-token sequence: every o_t and the final state."""
+    B, H, T, d = 1, 2, 24, 128
+    w = Workload("chain", backbone, dtype, B, H, T, d, d, 64, 5, "iso")
+    inp = make_inputs(w)
+    S = torch.zeros((B, H, d, d), device="cuda")
+    C = torch.zeros((B, H, d, d), device="cuda")
+    m = torch.zeros((B, H, d), device="cuda")
+    wl, bl = inp["w_lambda"].cuda(), inp["b_lambda"].cuda()
+    outs = [_step(backbone, _token(inp, t), S, C, m, t, wl, bl) for t in range(T)]
+    torch.cuda.synchronize()
+    o = np.stack([np64(x) for x in outs], axis=2)
+    ref = oracle.run(backbone, inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["w_lambda"],
+                     inp["b_lambda"], beta=inp.get("beta"))
+    check(o, ref["o"], dtype, "chained o")
+    for key, got in (("S", S), ("C", C), ("m", m)):
+        check(np64(got), ref[key], "f32", "chained " + key, per_head=False)
+
+
+@pytest.mark.parametrize("backbone", ["gla", "gdn"])
+@pytest.mark.parametrize("lam", [0.0, 0.25])
+def test_step_given_lambda(backbone, lam):
+    B, H, d = 2, 2, 128
+    w = Workload("lam", backbone, "bf16", B, H, 1, d, d, 64, 8, "iso")
+    inp = make_inputs(w)
+    S0, C0, m0 = _state(np.random.default_rng(3), B, H, d, d, 50)
+    S, C, m = (torch.from_numpy(x).cuda() for x in (S0, C0, m0))
+    lin = np.full((B, H), lam, np.float32)
+    lout = torch.empty((B, H), dtype=torch.float32, device="cuda")
+    o = _step(backbone, _token(inp, 0), S, C, m, 50, None, None,
+              lambda_in=torch.from_numpy(lin).cuda(), lambda_out=lout)
+    torch.cuda.synchronize()
+    ref = _oracle_one(backbone, inp, 0, S0, C0, m0, 50, lambda_in=lin[:, :, None])
+    check(np64(o), ref["o"][:, :, 0], "bf16", f"lambda={lam} o")
+    np.testing.assert_array_equal(np64(lout), lin)
+
+
+def test_step_l2norm_flag():
+    B, H, d = 1, 3, 128
+    w = Workload("l2", "gla", "bf16", B, H, 1, d, d, 64, 9, "iso")
+    inp = make_inputs(w)
+    g = torch.Generator().manual_seed(1)
+    inp["q"] = (torch.randn(inp["q"].shape, generator=g) * 3).to(torch.bfloat16)
+    inp["k"] = (torch.randn(inp["k"].shape, generator=g) * 3).to(torch.bfloat16)
+    S0, C0, m0 = _state(np.random.default_rng(4), B, H, d, d, 20)
+    S, C, m = (torch.from_numpy(x).cuda() for x in (S0, C0, m0))
+    o = _step("gla", _token(inp, 0), S, C, m, 20, inp["w_lambda"].cuda(), inp["b_lambda"].cuda(),
+              flags=ccq.FLAG_L2NORM_QK)
+    torch.cuda.synchronize()
+    ref = _oracle_one("gla", inp, 0, S0, C0, m0, 20, l2norm=True)
+    check(np64(o), ref["o"][:, :, 0], "bf16", "l2norm o")
+    check(np64(C), ref["C"], "f32", "l2norm C", per_head=False)
+
+
+@pytest.mark.parametrize("backbone", ["gla", "gdn"])
+def test_step_serving_batch_full_size(backbone):
+    """The benchmark's decode batch (B64 H16 d128, bf16), every head checked."""
+    B, H, d = 64, 16, 128
+    w = Workload("serve", backbone, "bf16", B, H, 1, d, d, 64, 11, "iso")
+    inp = make_inputs(w)
+    S0, C0, m0 = _state(np.random.default_rng(5), B, H, d, d, 16)
+    S, C, m = (torch.from_numpy(x).cuda() for x in (S0, C0, m0))
+    o = _step(backbone, _token(inp, 0), S, C, m, 4096, inp["w_lambda"].cuda(),
+              inp["b_lambda"].cuda())
+    torch.cuda.synchronize()
+    assert ccq.last_device_status() == 0
+    ref = _oracle_one(backbone, inp, 0, S0, C0, m0, 4096)
+    check(np64(o), ref["o"][:, :, 0], "bf16", "serving o")
+    for key, got in (("S", S), ("C", C), ("m", m)):
+        check(np64(got), ref[key], "f32", "serving " + key, per_head=False)
+
+
+def test_step_empty_batch_is_a_no_op():
+    z = torch.zeros((0, 4, 128), dtype=torch.bfloat16, device="cuda")
+    S = torch.zeros((0, 4, 128, 128), device="cuda")
+    m = torch.zeros((0, 4, 128), device="cuda")
+    o = ccq.gla_step(z, z, z, z, S, S, m, 0, torch.zeros((4, 128), device="cuda"),
+                     torch.zeros(4, device="cuda"))
+    torch.cuda.synchronize()
+    assert o.shape == (0, 4, 128)
