@@ -135,6 +135,7 @@ extern "C" ccq_status ccq_gla_step(const void *q, const void *k, const void *v,
     ccq_status s = check_step(q, k, v, log_alpha, w_lambda, b_lambda, lambda_in, o, S, C, m, t0,
                               B, H, dk, dv, dtype, flags);
     if (s != CCQ_OK) return s;
+    if ((long long)B * H == 0) return CCQ_OK;  // nothing to do, no CUDA call
     unsigned int *st_word = status_word();
     if (!st_word) return CCQ_ERR_CUDA;
     return to_status(launch_step(q, k, v, log_alpha, nullptr, w_lambda, b_lambda, lambda_in,
@@ -152,7 +153,8 @@ extern "C" ccq_status ccq_gdn_step(const void *q, const void *k, const void *v,
     ccq_status s = check_step(q, k, v, log_alpha, w_lambda, b_lambda, lambda_in, o, S, C, m, t0,
                               B, H, dk, dv, dtype, flags);
     if (s != CCQ_OK) return s;
-    if (!beta && (long long)B * H > 0) return CCQ_ERR_INVALID_ARG;
+    if ((long long)B * H == 0) return CCQ_OK;  // nothing to do, no CUDA call
+    if (!beta) return CCQ_ERR_INVALID_ARG;
     unsigned int *st_word = status_word();
     if (!st_word) return CCQ_ERR_CUDA;
     return to_status(launch_step(q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in,
