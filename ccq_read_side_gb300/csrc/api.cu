@@ -28,6 +28,17 @@ cudaError_t launch_simt(const CcqParams &p, bool gdn, bool bf16, cudaStream_t st
 // shape is not one it takes.
 cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st);
 bool tc_gla_supported(const CcqParams &p);
+// Tensor-core Gated DeltaNet forward in two passes: the covariance CTA writes
+// the cleaned query into o (tc_gla.cu), then the delta rule (gdn_rule.cu)
+// turns it into o in place.
+cudaError_t launch_tc_qclean(const CcqParams &p, cudaStream_t st);
+cudaError_t launch_gdn_rule(const CcqParams &p, cudaStream_t st);
+static bool tc_gdn_supported(const CcqParams &p) {
+    auto al = [](const void *x) { return ((uintptr_t)x & 15u) == 0; };
+    return p.dk == 128 && p.dv == 128 && p.T > 0 && p.B * p.H > 0 &&
+           !(p.flags & CCQ_FLAG_L2NORM_QK) && al(p.q) && al(p.k) && al(p.o) &&
+           (long long)p.B * p.H * 8 < 0x7fffffffLL;
+}
 // Single-token step (step.cu).
 cudaError_t launch_step(const void *q, const void *k, const void *v, const void *log_alpha,
                         const void *beta, const float *w_lambda, const float *b_lambda,
@@ -123,7 +134,13 @@ extern "C" ccq_status ccq_gdn_fwd(const void *q, const void *k, const void *v,
     p.status = status_word();
     if (!p.status) return CCQ_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return to_status(launch_simt(p, true, dtype == CCQ_DTYPE_BF16, st));
+    const bool bf16 = dtype == CCQ_DTYPE_BF16;
+    if (bf16 && !(flags & CCQ_FLAG_FP32_PATH) && tc_gdn_supported(p)) {
+        cudaError_t e = launch_tc_qclean(p, st);
+        if (e == cudaSuccess) e = launch_gdn_rule(p, st);
+        return to_status(e);
+    }
+    return to_status(launch_simt(p, true, bf16, st));
 }
 
 extern "C" ccq_status ccq_gla_step(const void *q, const void *k, const void *v,

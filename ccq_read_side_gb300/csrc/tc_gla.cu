@@ -233,7 +233,12 @@ __device__ __forceinline__ void mma_k_loop(uint32_t d, uint64_t adesc, uint32_t 
               A_MN ? 128 : 2, B_MN ? 128 : 2, idesc, NK / 4, acc0);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1)
+// QC = false: the CCQ-GLA forward, clusters of two CTAs (launched with the
+// cluster size set at launch).  QC = true: the covariance CTA alone (clusters
+// of one) writes the cleaned query qc itself (bf16, [B, H, T, dk]) to the
+// output tensor -- the first pass of the Gated DeltaNet forward.
+template <bool QC>
+__global__ void __launch_bounds__(NTHREADS, 1)
 tc_gla_kernel(const __grid_constant__ Args args) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -245,7 +250,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
-    const int bh = blockIdx.x >> 1, h = bh % p.H;
+    const int bh = QC ? (int)blockIdx.x : (int)(blockIdx.x >> 1), h = bh % p.H;
     const int T = p.T;
     const int nch = (T + L - 1) / L;
     volatile int *abort = &aux.abort;
@@ -286,9 +291,9 @@ tc_gla_kernel(const __grid_constant__ Args args) {
     }
     if (warp == WARP_TMA && lane == 0) {
         prefetch_tensormap(&args.mk);
-        prefetch_tensormap(&args.mla);
+        if (!QC) prefetch_tensormap(&args.mla);
         prefetch_tensormap(rank == 0 ? &args.mq : &args.mv);
-        if (rank == 1) prefetch_tensormap(&args.mo);
+        if (rank == 1 || QC) prefetch_tensormap(&args.mo);
     }
     if (warp == WARP_MMA) {
         tmem_alloc(smem_u32(&aux.tmem_base), TMEM_COLS);
@@ -324,7 +329,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 for (int b = 0; b < 2; ++b) {
                     tma_prefetch_3d(m0, b * 64, k * L, bh);
                     tma_prefetch_3d(m1, b * 64, k * L, bh);
-                    tma_prefetch_3d(m2, b * 64, k * L, bh);
+                    if (!QC) tma_prefetch_3d(m2, b * 64, k * L, bh);
                 }
             };
             for (int k = 0; k < 2 && k < nload; ++k) prefetch(k);
@@ -339,7 +344,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 if (n >= 2 && !mbar_wait(smem_u32(&aux.empty[s]), ((n >> 1) - 1) & 1, abort)) break;
                 CCQ_TRACE(2, n, 0);
                 const uint32_t fb = smem_u32(&aux.full[s]);
-                mbar_expect_tx(fb, (rank == 0 ? 3 : 2) * TILE);
+                mbar_expect_tx(fb, (rank == 0 && !QC ? 3 : 2) * TILE);
                 for (int b = 0; b < 2; ++b) {
                     tma_load_3d(smem_u32(smem + s * TILE + b * BOX), m0, fb, b * 64, n * L, bh);
                     tma_load_3d(smem_u32(smem + base1 + s * stage1 + b * blk1), m1, fb, b * 64,
@@ -352,9 +357,10 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     f2 = smem_u32(&aux.vfull[s]);
                     mbar_expect_tx(f2, TILE);
                 }
-                for (int b = 0; b < 2; ++b)
-                    tma_load_3d(smem_u32(smem + base2 + s * TILE + b * BOX), m2, f2, b * 64, n * L,
-                                bh);
+                if (!QC)  // (the cleaned query needs no log alpha)
+                    for (int b = 0; b < 2; ++b)
+                        tma_load_3d(smem_u32(smem + base2 + s * TILE + b * BOX), m2, f2, b * 64,
+                                    n * L, bh);
             }
         }
         __syncwarp();
@@ -395,8 +401,9 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     mma_k_loop<true, true, 4>(tmem + C_COL, sw128_desc(sK, KBLK, 1024), 0,
                                               sw128_desc(sK, KBLK, 1024), 0, ID_M128N128_MM, 1);
                     // E^T = LA^T U^T
-                    mma_k_loop<true, false, 4>(tmem + E0_COL, sw128_desc(sLA, BOX, 1024), 0,
-                                               sw128_desc(sUX, 0, 1024), 0, ID_M128N64_MK, 0);
+                    if (!QC)
+                        mma_k_loop<true, false, 4>(tmem + E0_COL, sw128_desc(sLA, BOX, 1024), 0,
+                                                   sw128_desc(sUX, 0, 1024), 0, ID_M128N64_MK, 0);
                     CCQ_TRACE(1, n, 8);
                     if (!mbar_wait(smem_u32(&aux.ahat_ready), n & 1, abort)) break;
                     tc_fence_after();
@@ -626,21 +633,29 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     const int i0 = 16 * qt + 8 * g;
                     uint32_t pr[8], er[8];
                     tmem_ld8(tl + P_COL(b) + i0, pr);
-                    tmem_ld8(tl + E0_COL + i0, er);
+                    if (!QC) tmem_ld8(tl + E0_COL + i0, er);
                     float qv[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) qv[e] = bf16_at(sQs, i0 + e, c, 64);
                     tmem_ld_wait();
                     if (tid == 0 && g == 0) CCQ_TRACE(0, n, 9);
-                    if (i0 == 0 && u2f(er[0]) < -80.f) record_status(p.status, CCQ_ERR_RANGE);
                     float v[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float2 tk = aux.tok[i0 + e];
-                        const float qc = qv[e] - tk.x * (u2f(pr[e]) - tk.y * m_cur);
-                        v[e] = qc * exp2f(-1.4426950408889634f * u2f(er[e]));
+                        v[e] = qv[e] - tk.x * (u2f(pr[e]) - tk.y * m_cur);
                     }
-                    store8(qtb + sw128_chunk(c, i0, 128), v);
+                    if (QC) {
+                        // qc itself, token-major (the output tensor's tile layout)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) put_bf16(qtb + sw128_off(i0 + e, c, 64), v[e]);
+                    } else {
+                        if (i0 == 0 && u2f(er[0]) < -80.f) record_status(p.status, CCQ_ERR_RANGE);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            v[e] *= exp2f(-1.4426950408889634f * u2f(er[e]));
+                        store8(qtb + sw128_chunk(c, i0, 128), v);
+                    }
                 }
                 if (tid == 0) CCQ_TRACE(2, n, 5);
                 if (more) {
@@ -668,8 +683,14 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 CCQ_TRACE(0, n, 10);
                 if (more) mbar_arrive(smem_u32(&aux.c0_ready));
                 mbar_arrive(smem_u32(&aux.empty[b]));  // stage b: MMAs done (p_full), Q, K read
-                bool sent = true;
-                if (n >= 2)
+                if (QC) {
+                    const uint32_t sq = smem_u32(smem + CovLayout::QT + b * 16384);
+                    tma_store_3d(&args.mo, sq, 0, c0t, bh);
+                    tma_store_3d(&args.mo, sq + BOX, 64, c0t, bh);
+                    bulk_commit();
+                }
+                bool sent = !QC;
+                if (!QC && n >= 2)
                     sent = mbar_wait(smem_u32(&aux.qt_empty[b]), ((n >> 1) - 1) & 1, abort, true);
                 if (sent) {
                     const uint32_t rfull = mapa(smem_u32(&aux.qt_full[b]), 1);
@@ -944,14 +965,16 @@ bool tc_gla_supported(const CcqParams &p) {
            al(p.log_alpha) && al(p.o) && (long long)p.B * p.H * 2 < 0x7fffffffLL;
 }
 
-cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st) {
+template <bool QC>
+static cudaError_t launch_tc(const CcqParams &p, cudaStream_t st) {
     using namespace tcgla;
     Args a;
     a.p = p;
     const int BH = p.B * p.H;
     if (!make_map(&a.mq, p.q, p.T, BH) || !make_map(&a.mk, p.k, p.T, BH) ||
-        !make_map(&a.mv, p.v, p.T, BH) || !make_map(&a.mla, p.log_alpha, p.T, BH) ||
         !make_map(&a.mo, p.o, p.T, BH))
+        return cudaErrorInvalidValue;
+    if (!QC && (!make_map(&a.mv, p.v, p.T, BH) || !make_map(&a.mla, p.log_alpha, p.T, BH)))
         return cudaErrorInvalidValue;
     // The dynamic shared-memory limit is a per-device function attribute.
     int dev = 0;
@@ -960,13 +983,31 @@ cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st) {
     static bool attr_set[64] = {};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(tc_gla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(tc_gla_kernel<QC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    tc_gla_kernel<<<2 * BH, NTHREADS, SMEM_BYTES, st>>>(a);
-    return cudaGetLastError();
+    const unsigned cl = QC ? 1u : 2u;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cl * (unsigned)BH);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tc_gla_kernel<QC>, a);
 }
+
+cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st) { return launch_tc<false>(p, st); }
+
+// First pass of the tensor-core Gated DeltaNet forward: qc (bf16) into p.o,
+// plus lambda_out, C_out and m_out.
+cudaError_t launch_tc_qclean(const CcqParams &p, cudaStream_t st) { return launch_tc<true>(p, st); }
 
 }  // namespace ccq
