@@ -8,19 +8,25 @@
 //     S_t = alpha_t (S_{t-1} - beta_t k_t (k_t^T S_{t-1})) + beta_t k_t v_t^T,
 // treats every column of S independently: column j only ever meets v_{t,j}
 // and o_{t,j} = S_t[:, j] . qc_t.  So the d_v columns are split over a
-// cluster of NC CTAs per (b, h), each keeping its dk x (dv / NC) slice of S
-// in shared memory for the whole sequence.  Per chunk of L tokens (scalar
+// cluster of NC CTAs per (b, h), each keeping its dk x W slice of S (W =
+// dv / NC = 16) for the whole sequence.  Per chunk of L = 16 tokens (scalar
 // cumulative log-decay g, Gam_il = exp(g_i - g_l)), the chunk form
 //     Aw = strict_tril(beta_i Gam_il k_i . k_l),  Ag = tril(Gam_il qc_i . k_l)
 //     U  = (I + Aw)^-1 (beta V - beta exp(g) (K S0))
 //     O  = exp(g) (Qc S0) + Ag U
 //     S <- exp(g_L) S0 + (K exp(g_L - g))^T U
-// is evaluated for the CTA's columns; the L x L matrices are computed by
-// every CTA of the cluster (they do not depend on S).
+// is evaluated for the CTA's columns.  The four 16 x 16 x 128 products (K K^T,
+// Qc K^T, K S0, Qc S0) and the state update (128 x 16 x 16) run on the
+// tensor cores through warp-level mma.sync (bf16 operands, fp32
+// accumulation); the state slice itself stays in fp32 registers (one 16-row
+// band per warp) for the whole sequence, and a bf16 copy in shared memory
+// feeds the next chunk's products.  The unit-lower-triangular solve for U is a
+// register-resident forward substitution, one lane per column.  Each chunk's
+// inputs are loaded into registers while the previous chunk computes.
 //
-// qc and o share the output tensor: a cluster barrier after each chunk's
-// loads guarantees that every CTA has read the chunk's qc rows before any CTA
-// overwrites them with o.
+// qc and o share the output tensor: a cluster barrier per chunk (arrive once
+// the chunk's qc is in shared memory, wait before the first o store)
+// guarantees that every CTA has read it before any CTA overwrites it with o.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -31,142 +37,250 @@ namespace gdnrule {
 
 constexpr int NC = 8;          // CTAs per (b, h)
 constexpr int L = 16;          // tokens per chunk
-constexpr int NTHREADS = 256;
+constexpr int DK = 128, DV = 128;
+constexpr int W = DV / NC;     // columns of S per CTA (16)
+constexpr int NTHREADS = 256;  // 8 warps: warp w owns rows [16w, 16w+16) of the S slice
+// Shared rows are padded by 16 bytes: 256-byte rows would put the eight rows
+// an mma fragment reads in the same banks.
+constexpr int DKP = DK + 8;
 
-template <typename TIn, int DK, int DV>
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+__device__ __forceinline__ float bf(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+
+// D += A B for one m16n8k16 tile: A 16 x 16 (row-major fragment), B 16 x 8.
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4],
+                                         const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+struct Smem {
+    __nv_bfloat16 K[L][DKP];     // chunk tiles (rows padded)
+    __nv_bfloat16 Q[L][DKP];     // qc
+    __nv_bfloat16 St[W][DKP];    // bf16 copy of the S slice, transposed ([column][row])
+    __nv_bfloat16 Ut[W][L];      // bf16 U, transposed
+    float V[L][W];
+    float la[L], beta[L];
+    float Aw[L][L], Ag[L][L];
+    float X[L][W], QS[L][W], U[L][W];
+    float G[L], E[L], Dd[L];
+};
+
+// One chunk's inputs as loaded by one thread: 16 bytes of a K row and of a qc
+// row (row tid / 16, part tid % 16), one V element, and (tid < 16) log alpha
+// and beta of one token.  Loads past the tail read the last valid token
+// instead (always in bounds) and are zeroed only when stored, a chunk later:
+// selecting on a loaded value would make the thread wait for the load.
+struct Chunk {
+    uint4 k, q;
+    __nv_bfloat16 v, la, beta;
+};
+
 __global__ void __cluster_dims__(NC, 1, 1) __launch_bounds__(NTHREADS)
 gdn_rule_kernel(const __grid_constant__ CcqParams p) {
-    constexpr int W = DV / NC;  // columns of S in this CTA
-    static_assert(L * L == NTHREADS, "one thread per (i, l) of the chunk's L x L matrices");
-    static_assert(L * W <= NTHREADS, "one thread per (i, j) of the chunk's L x W tiles");
-    __shared__ float sS[DK][W];
-    __shared__ float sK[L][DK + 1], sQ[L][DK + 1];  // +1: conflict-free row-wise dots
-    __shared__ float sV[L][W], sX[L][W], sU[L][W], sQS[L][W];
-    __shared__ float sAw[L][L], sAg[L][L];
-    __shared__ float sLa[L], sBeta[L], sG[L], sE[L], sD[L];
-
-    const int tid = threadIdx.x;
+    __shared__ __align__(128) Smem sm;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g4 = lane >> 2, t4 = lane & 3;  // mma fragment coordinates
     const uint32_t rank = sm103::cluster_ctarank();
     const int bh = blockIdx.x / NC;
     const int j0 = (int)rank * W;
     const int T = p.T;
-    const TIn *gk = static_cast<const TIn *>(p.k) + (size_t)bh * T * DK;
-    const TIn *gv = static_cast<const TIn *>(p.v) + (size_t)bh * T * DV;
-    const TIn *gla = static_cast<const TIn *>(p.log_alpha) + (size_t)bh * T;
-    const TIn *gbeta = static_cast<const TIn *>(p.beta) + (size_t)bh * T;
-    TIn *go = static_cast<TIn *>(p.o) + (size_t)bh * T * DV;  // qc in, o out (DV == DK)
+    const int nch = (T + L - 1) / L;
+    const __nv_bfloat16 *gk = static_cast<const __nv_bfloat16 *>(p.k) + (size_t)bh * T * DK;
+    const __nv_bfloat16 *gv = static_cast<const __nv_bfloat16 *>(p.v) + (size_t)bh * T * DV;
+    const __nv_bfloat16 *gla = static_cast<const __nv_bfloat16 *>(p.log_alpha) + (size_t)bh * T;
+    const __nv_bfloat16 *gbeta = static_cast<const __nv_bfloat16 *>(p.beta) + (size_t)bh * T;
+    __nv_bfloat16 *go = static_cast<__nv_bfloat16 *>(p.o) + (size_t)bh * T * DV;
 
-    for (int x = tid; x < DK * W; x += NTHREADS) {
-        const int c = x / W, j = x % W;
-        sS[c][j] = p.S0 ? p.S0[((size_t)bh * DK + c) * DV + j0 + j] : 0.f;
-    }
-
-    for (int c0 = 0; c0 < T; c0 += L) {
-        const int Lc = min(L, T - c0);
-        // ---- the chunk: K, qc (zero past the tail), this CTA's columns of V
-        for (int x = tid; x < L * DK; x += NTHREADS) {
-            const int i = x / DK, c = x % DK;
-            const bool ok = i < Lc;
-            sK[i][c] = ok ? io<TIn>::load(gk + (size_t)(c0 + i) * DK + c) : 0.f;
-            sQ[i][c] = ok ? io<TIn>::load(go + (size_t)(c0 + i) * DV + c) : 0.f;
-        }
-        if (tid < L * W) {
-            const int i = tid / W, j = tid % W;
-            sV[i][j] = i < Lc ? io<TIn>::load(gv + (size_t)(c0 + i) * DV + j0 + j) : 0.f;
-        }
+    auto fetch = [&](int c) {
+        const int last = T - 1 - c * L;  // last valid row of the chunk
+        const int r = min(tid >> 4, last), part = tid & 15;
+        const size_t row = (size_t)c * L + r;
+        Chunk x;
+        x.k = *reinterpret_cast<const uint4 *>(gk + row * DK + 8 * part);
+        x.q = *reinterpret_cast<const uint4 *>(go + row * DV + 8 * part);
+        const int i = min(tid / W, last), j = tid % W, t = min(tid & (L - 1), last);
+        x.v = gv[(size_t)(c * L + i) * DV + j0 + j];
+        x.la = gla[c * L + t];
+        x.beta = gbeta[c * L + t];
+        return x;
+    };
+    auto store = [&](const Chunk &x, int c) {
+        const int lc = min(L, T - c * L);
+        const int r = tid >> 4, part = tid & 15;
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(&sm.K[r][8 * part]) = r < lc ? x.k : z;
+        *reinterpret_cast<uint4 *>(&sm.Q[r][8 * part]) = r < lc ? x.q : z;
+        sm.V[tid / W][tid % W] = tid / W < lc ? __bfloat162float(x.v) : 0.f;
         if (tid < L) {
-            const bool ok = tid < Lc;
-            sLa[tid] = ok ? io<TIn>::load(gla + c0 + tid) : 0.f;
-            sBeta[tid] = ok ? io<TIn>::load(gbeta + c0 + tid) : 0.f;
+            sm.la[tid] = tid < lc ? __bfloat162float(x.la) : 0.f;
+            sm.beta[tid] = tid < lc ? __bfloat162float(x.beta) : 0.f;
         }
-        __syncthreads();
-        // every CTA of the cluster holds this chunk's qc: o may now overwrite it
-        sm103::cluster_sync();
+    };
 
-        // ---- scalar cumulative log-decay (zero past the tail)
-        if (tid < 32) {
-            float g = tid < L ? sLa[tid] : 0.f;
+    // ---- S slice: warp w holds rows [16w, 16w+16) x 16 columns as two m16n8
+    // accumulator tiles; its bf16 transposed copy feeds K S0 and Qc S0
+    float sacc[2][4];
+    {
+        const int r0 = 16 * warp;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = r0 + g4 + 8 * (e >> 1), j = 8 * nt + 2 * t4 + (e & 1);
+                sacc[nt][e] = p.S0 ? p.S0[((size_t)bh * DK + r) * DV + j0 + j] : 0.f;
+                sm.St[j][r] = __float2bfloat16_rn(sacc[nt][e]);
+            }
+    }
+    if (nch > 0) store(fetch(0), 0);
+    __syncthreads();
+    // this CTA holds chunk 0's qc; o may overwrite a chunk's qc once every CTA
+    // of the cluster has said so (each wait sits just before the chunk's first
+    // o store; an arrive follows the loads, so it is relaxed)
+    if (nch > 0) sm103::cluster_arrive_relaxed();
+
+    for (int c = 0; c < nch; ++c) {
+        const int c0 = c * L, lc = min(L, T - c0);
+        // next chunk's inputs: in flight while this chunk computes
+        Chunk nxt{};
+        if (c + 1 < nch) nxt = fetch(c + 1);
+
+        // ---- cumulative log-decay of the chunk (one warp, shuffle scan)
+        if (warp == 0) {
+            float g = lane < L ? sm.la[lane] : 0.f;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, g, o);
-                if ((tid & 31) >= o) g += y;
+                if (lane >= o) g += y;
             }
-            if (tid < L) sG[tid] = g;
+            if (lane < L) sm.G[lane] = g;
         }
         __syncthreads();
-        const float gL = sG[L - 1];
+        const float gL = sm.G[L - 1];
         if (tid < L) {
-            sE[tid] = expf(sG[tid]);
-            sD[tid] = expf(gL - sG[tid]);
+            sm.E[tid] = expf(sm.G[tid]);
+            sm.Dd[tid] = expf(gL - sm.G[tid]);
         }
-        // ---- Aw_il = beta_i Gam_il k_i.k_l (l < i), Ag_il = Gam_il qc_i.k_l (l <= i)
+
+        // ---- four 16 x 8 tiles per product over k = 128: warp (prod, nt)
         {
-            const int i = tid / L, l = tid % L;
-            float aw = 0.f, ag = 0.f;
-            if (i < Lc && l <= i) {
-                float kk = 0.f, qk = 0.f;
-#pragma unroll 8
-                for (int d = 0; d < DK; ++d) {
-                    const float kl = sK[l][d];
-                    kk += sK[i][d] * kl;
-                    qk += sQ[i][d] * kl;
-                }
-                const float gam = expf(sG[i] - sG[l]);
-                ag = gam * qk;
-                if (l < i) aw = sBeta[i] * gam * kk;
-            }
-            sAw[i][l] = aw;
-            sAg[i][l] = ag;
-        }
-        // ---- X = beta V - beta exp(g) (K S0);  QS = Qc S0  (this CTA's columns)
-        if (tid < L * W) {
-            const int i = tid / W, j = tid % W;
-            float ks = 0.f, qs = 0.f;
-#pragma unroll 8
-            for (int c = 0; c < DK; ++c) {
-                const float s = sS[c][j];
-                ks += sK[i][c] * s;
-                qs += sQ[i][c] * s;
-            }
-            sQS[i][j] = qs;
-            sX[i][j] = sBeta[i] * (sV[i][j] - expf(sG[i]) * ks);
-        }
-        __syncthreads();
-        // ---- U = (I + Aw)^-1 X, forward substitution down each column
-        if (tid < W) {
-            const int j = tid;
-            for (int i = 0; i < L; ++i) {
-                float u = sX[i][j];
-                for (int l = 0; l < i; ++l) u -= sAw[i][l] * sU[l][j];
-                sU[i][j] = u;
-            }
-        }
-        __syncthreads();
-        // ---- O = exp(g) QS + Ag U
-        if (tid < L * W) {
-            const int i = tid / W, j = tid % W;
-            if (i < Lc) {
-                float a = sE[i] * sQS[i][j];
-                for (int l = 0; l <= i; ++l) a += sAg[i][l] * sU[l][j];
-                io<TIn>::store(go + (size_t)(c0 + i) * DV + j0 + j, a);
-            }
-        }
-        // ---- S <- exp(g_L) S + (K exp(g_L - g))^T U
-        const float egL = expf(gL);
-        for (int x = tid; x < DK * W; x += NTHREADS) {
-            const int c = x / W, j = x % W;
-            float a = egL * sS[c][j];
+            const int prod = warp >> 1, nt = warp & 1;  // 0 KK^T, 1 QK^T, 2 K S0, 3 Q S0
+            const __nv_bfloat16(*A)[DKP] = (prod == 1 || prod == 3) ? sm.Q : sm.K;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < L; ++i) a += sK[i][c] * sD[i] * sU[i][j];
-            sS[c][j] = a;
+            for (int ks = 0; ks < DK / 16; ++ks) {
+                const int k0 = 16 * ks + 2 * t4;
+                uint32_t a[4], bb[2];
+                a[0] = *reinterpret_cast<const uint32_t *>(&A[g4][k0]);
+                a[1] = *reinterpret_cast<const uint32_t *>(&A[g4 + 8][k0]);
+                a[2] = *reinterpret_cast<const uint32_t *>(&A[g4][k0 + 8]);
+                a[3] = *reinterpret_cast<const uint32_t *>(&A[g4 + 8][k0 + 8]);
+                const int n = 8 * nt + g4;
+                const __nv_bfloat16 *brow = prod < 2 ? &sm.K[n][0] : &sm.St[n][0];
+                bb[0] = *reinterpret_cast<const uint32_t *>(brow + k0);
+                bb[1] = *reinterpret_cast<const uint32_t *>(brow + k0 + 8);
+                mma16816(d, a, bb);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int i = g4 + 8 * (e >> 1), n = 8 * nt + 2 * t4 + (e & 1);
+                const bool row_ok = i < lc;
+                if (prod == 0) {
+                    sm.Aw[i][n] = (row_ok && n < i)
+                                      ? sm.beta[i] * expf(sm.G[i] - sm.G[n]) * d[e] : 0.f;
+                } else if (prod == 1) {
+                    sm.Ag[i][n] = (row_ok && n <= i) ? expf(sm.G[i] - sm.G[n]) * d[e] : 0.f;
+                } else if (prod == 2) {
+                    sm.X[i][n] = row_ok ? sm.beta[i] * (sm.V[i][n] - expf(sm.G[i]) * d[e]) : 0.f;
+                } else {
+                    sm.QS[i][n] = d[e];
+                }
+            }
         }
         __syncthreads();
-    }
-    if (p.S_out)
-        for (int x = tid; x < DK * W; x += NTHREADS) {
-            const int c = x / W, j = x % W;
-            p.S_out[((size_t)bh * DK + c) * DV + j0 + j] = sS[c][j];
+
+        // ---- U = (I + Aw)^-1 X: lane j of warp 0 walks column j down the rows
+        if (warp == 0 && lane < W) {
+            const int j = lane;
+            float u[L];
+#pragma unroll
+            for (int i = 0; i < L; ++i) {
+                float x = sm.X[i][j];
+#pragma unroll
+                for (int l = 0; l < i; ++l) x -= sm.Aw[i][l] * u[l];
+                u[i] = x;
+                sm.U[i][j] = x;
+                sm.Ut[j][i] = __float2bfloat16_rn(x);
+            }
         }
+        __syncthreads();
+
+        // ---- O = exp(g) QS + Ag U (fp32, one (i, j) per thread)
+        sm103::cluster_wait();  // every CTA holds this chunk's qc
+        {
+            const int i = tid / W, j = tid % W;
+            if (i < lc) {
+                float a = sm.E[i] * sm.QS[i][j];
+#pragma unroll
+                for (int l = 0; l < L; ++l) a += sm.Ag[i][l] * sm.U[l][j];
+                go[(size_t)(c0 + i) * DV + j0 + j] = __float2bfloat16_rn(a);
+            }
+        }
+        // ---- S <- exp(g_L) S + (K exp(g_L - g))^T U: warp w, rows [16w, 16w+16)
+        {
+            const float egL = expf(gL);
+            const int r0 = 16 * warp;
+            uint32_t a[4];
+            // A[m][k] = K[k][r0 + m] * d_k  (m: state row, k: token)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int m = g4 + 8 * (q & 1), k = 2 * t4 + 8 * (q >> 1);
+                a[q] = pack_bf16(bf(&sm.K[k][r0 + m]) * sm.Dd[k],
+                                 bf(&sm.K[k + 1][r0 + m]) * sm.Dd[k + 1]);
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                uint32_t bb[2];
+                const __nv_bfloat16 *ucol = &sm.Ut[8 * nt + g4][0];
+                bb[0] = *reinterpret_cast<const uint32_t *>(ucol + 2 * t4);
+                bb[1] = *reinterpret_cast<const uint32_t *>(ucol + 2 * t4 + 8);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[nt][e] *= egL;
+                mma16816(sacc[nt], a, bb);
+            }
+        }
+        __syncthreads();  // this chunk no longer reads K, Q, V, St
+        {
+            const int r0 = 16 * warp;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = r0 + g4 + 8 * (e >> 1), j = 8 * nt + 2 * t4 + (e & 1);
+                    sm.St[j][r] = __float2bfloat16_rn(sacc[nt][e]);
+                }
+        }
+        if (c + 1 < nch) store(nxt, c + 1);
+        __syncthreads();
+        if (c + 1 < nch) sm103::cluster_arrive_relaxed();  // this CTA holds chunk c+1's qc
+    }
+    if (p.S_out) {
+        const int r0 = 16 * warp;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int r = r0 + g4 + 8 * (e >> 1), j = 8 * nt + 2 * t4 + (e & 1);
+                p.S_out[((size_t)bh * DK + r) * DV + j0 + j] = sacc[nt][e];
+            }
+    }
+    sm103::cluster_sync();  // no CTA leaves while a peer may still be at a barrier
 }
 
 }  // namespace gdnrule
@@ -175,7 +289,7 @@ gdn_rule_kernel(const __grid_constant__ CcqParams p) {
 cudaError_t launch_gdn_rule(const CcqParams &p, cudaStream_t st) {
     using namespace gdnrule;
     if (p.B * p.H == 0 || p.T == 0) return cudaSuccess;
-    gdn_rule_kernel<__nv_bfloat16, 128, 128><<<p.B * p.H * NC, NTHREADS, 0, st>>>(p);
+    gdn_rule_kernel<<<p.B * p.H * NC, NTHREADS, 0, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -120,6 +120,17 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of a cluster barrier, issued apart so that work between
+// them hides the wait.  The arrive is relaxed: it orders nothing by itself,
+// for hand-offs whose data dependence is already settled (e.g. every CTA has
+// seen its bulk copy land before arriving).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ proxies
 __device__ __forceinline__ void fence_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
