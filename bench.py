@@ -2,13 +2,15 @@
 fp32 state) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gla_fwd|gdn_fwd|gla_step|gdn_step]
+                    [--workload gla_fwd|gdn_fwd|gla_step|gdn_step|ccq_overhead]
 
 Default (the headline): one step = one CCQ-GLA forward over the whole batch
 (read + gate + stats + GLA write/read, final state written).  The other
 workloads measure the rest of the library on their own JSON line: the Gated
 DeltaNet forward (B2 H16 T8192 d128) and the single-token decode steps
-(B64 H16 d128, state resident on the device and updated in place).  Inputs are seeded synthetic data with
+(B64 H16 d128, state resident on the device and updated in place).
+ccq_overhead sweeps T = 2K..32K (B4 H16 d128) and reports the time of the
+CCQ-GLA forward over the plain GLA forward on the same pipeline.  Inputs are seeded synthetic data with
 the workload's distributions (anisotropic keys with one needle per sequence).
 For N > 1 (launched by torch.distributed.run) every rank runs its own replica
 of the workload on its own GPU (weak scaling, no collective on the data path);
@@ -353,6 +355,77 @@ def run_ours(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_overhead(args, world, rank, local):
+    """CCQ-GLA forward vs the plain GLA forward (CCQ_FLAG_PLAIN_GLA) at growing
+    T, B4 H16 d128 bf16; timing only (parity is the tests' job), so the inputs
+    are drawn on the device with the benchmark workload's distributions."""
+    import ccq_read_side_gb300 as ccq
+
+    B, H, d = 4, 16, 128
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    prop = torch.cuda.get_device_properties(dev)
+    l2 = getattr(prop, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
+    flush = torch.empty(int(2 * l2) // 4, dtype=torch.int32, device=dev)
+    g = torch.Generator(device=dev).manual_seed(2)
+    wl = torch.randn((H, d), generator=g, device=dev) / d ** 0.5
+    bl = torch.zeros(H, device=dev)
+    rows = []
+    with ClockSampler(dev.index) as clk:
+        for T in (2048, 4096, 8192, 16384, 32768):
+            def unit(shape):
+                x = torch.randn(shape, generator=g, device=dev)
+                return torch.nn.functional.normalize(x, dim=-1).to(torch.bfloat16)
+            q, k = unit((B, H, T, d)), unit((B, H, T, d))
+            v = torch.randn((B, H, T, d), generator=g, device=dev).to(torch.bfloat16)
+            la = (torch.nn.functional.logsigmoid(torch.randn((B, H, T, d), generator=g,
+                                                             device=dev)) / 16).to(torch.bfloat16)
+            o = torch.empty_like(v)
+            times = {}
+            for mode in ("ccq", "plain"):
+                def fwd():
+                    if mode == "ccq":
+                        ccq.gla_fwd(q, k, v, la, wl, bl, o=o, want_state=False, stream=stream)
+                    else:
+                        ccq.gla_fwd(q, k, v, la, o=o, want_state=False,
+                                    flags=ccq.FLAG_PLAIN_GLA, stream=stream)
+                for _ in range(args.warmup):
+                    fwd()
+                ts = []
+                for _ in range(args.steps):
+                    flush.zero_()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fwd()
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e-3)
+                times[mode] = statistics.median(ts)
+            if ccq.last_device_status() != 0:
+                raise RuntimeError("device status after the sweep")
+            tok = B * T
+            rows.append({"T": T, "ccq_ms": times["ccq"] * 1e3, "plain_ms": times["plain"] * 1e3,
+                         "ratio": times["ccq"] / times["plain"],
+                         "ccq_us_per_ktoken": times["ccq"] / tok * 1e9,
+                         "plain_us_per_ktoken": times["plain"] / tok * 1e9})
+            del q, k, v, la, o
+    if rank != 0:
+        return
+    ratios = [r["ratio"] for r in rows]
+    line = {
+        "metric": "CCQ-GLA fwd time / plain GLA fwd time (same pipeline), B4 H16 d128, T 2K-32K",
+        "value": statistics.mean(ratios), "unit": "x", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (drawn on the device)",
+        "config": {"workload": "gla_bf16_b4h16d128_tsweep", "B": B, "H": H, "dk": d, "dv": d,
+                   "T": [r["T"] for r in rows],
+                   "l2": "flushed (2x L2 memset) before every timed forward; median of steps"},
+        "sweep": rows, "gpu_launches": 2 * len(rows) * args.steps, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def ccq_launches_per_step() -> int:
     return 1  # one fused kernel launch per forward (or per decode step)
 
@@ -509,8 +582,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["gla_fwd", "gdn_fwd", "gla_step", "gdn_step"],
-                    default="gla_fwd")
+    ap.add_argument("--workload", choices=["gla_fwd", "gdn_fwd", "gla_step", "gdn_step",
+                                           "ccq_overhead"], default="gla_fwd")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -520,6 +593,8 @@ def main():
             run_reference(args, world, rank)
         elif args.workload.endswith("_step"):
             run_step(args, world, rank, local)
+        elif args.workload == "ccq_overhead":
+            run_overhead(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

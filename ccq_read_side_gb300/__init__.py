@@ -17,13 +17,15 @@ from typing import Dict, Optional, Tuple
 import torch
 
 __all__ = ["gla_fwd", "gdn_fwd", "gla_step", "gdn_step", "last_device_status", "status_string", "CcqError",
-           "library", "FLAG_L2NORM_QK", "FLAG_FP32_PATH", "FLAG_TEST_STALL", "STATUS"]
+           "library", "FLAG_L2NORM_QK", "FLAG_FP32_PATH", "FLAG_PLAIN_GLA", "FLAG_TEST_STALL",
+           "STATUS"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libccq.so")
 
 FLAG_L2NORM_QK = 1
 FLAG_FP32_PATH = 2
+FLAG_PLAIN_GLA = 4  # measurement baseline: plain GLA read, no key statistics
 FLAG_TEST_STALL = 0x100  # test only: makes the tensor-core kernel's bounded waits run out
 STATUS = {0: "CCQ_OK", 1: "CCQ_ERR_INVALID_ARG", 2: "CCQ_ERR_UNSUPPORTED", 3: "CCQ_ERR_CUDA",
           4: "CCQ_ERR_TIMEOUT", 5: "CCQ_ERR_RANGE"}
@@ -128,8 +130,9 @@ def _fwd(backbone, q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in, S0, 
     S = C = m = None
     if want_state:
         S = torch.empty((B, H, dk, dv), dtype=torch.float32, device=dev)
-        C = torch.empty((B, H, dk, dk), dtype=torch.float32, device=dev)
-        m = torch.empty((B, H, dk), dtype=torch.float32, device=dev)
+        if not flags & FLAG_PLAIN_GLA:  # the plain baseline keeps no key statistics
+            C = torch.empty((B, H, dk, dk), dtype=torch.float32, device=dev)
+            m = torch.empty((B, H, dk), dtype=torch.float32, device=dev)
     lib = library()
     tail = (_ptr(S0), _ptr(C0), _ptr(m0), int(t0), _ptr(S), _ptr(C), _ptr(m), B, H, T, dk, dv,
             int(chunk), _DTYPES[dt], int(flags), _stream(stream))

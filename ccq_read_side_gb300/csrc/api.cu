@@ -27,6 +27,7 @@ cudaError_t launch_simt(const CcqParams &p, bool gdn, bool bf16, cudaStream_t st
 // Tensor-core GLA path (tc_gla.cu).  Returns cudaErrorNotSupported when the
 // shape is not one it takes.
 cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st);
+cudaError_t launch_tc_gla_plain(const CcqParams &p, cudaStream_t st);
 bool tc_gla_supported(const CcqParams &p);
 // Tensor-core Gated DeltaNet forward in two passes: the covariance CTA writes
 // the cleaned query into o (tc_gla.cu), then the delta rule (gdn_rule.cu)
@@ -51,13 +52,21 @@ static ccq_status check_common(const CcqParams &p, ccq_dtype dtype) {
     // Token tensors may be NULL only when there are no tokens to read.
     const bool has_tokens = p.T > 0 && p.B > 0 && p.H > 0;
     if (has_tokens && (!p.q || !p.k || !p.v || !p.log_alpha || !p.o)) return CCQ_ERR_INVALID_ARG;
-    if (has_tokens && !p.lambda_in && (!p.w_lambda || !p.b_lambda)) return CCQ_ERR_INVALID_ARG;
+    const bool plain = (p.flags & CCQ_FLAG_PLAIN_GLA) != 0;
+    if (has_tokens && !plain && !p.lambda_in && (!p.w_lambda || !p.b_lambda))
+        return CCQ_ERR_INVALID_ARG;
     int given = (p.S0 != nullptr) + (p.C0 != nullptr) + (p.m0 != nullptr);
+    if (plain) {  // no key statistics and no gate: only S may be carried
+        if (p.C0 || p.m0 || p.C_out || p.m_out || p.lambda_in || p.lambda_out)
+            return CCQ_ERR_INVALID_ARG;
+        given = p.S0 ? 3 : 0;
+    }
     if (given != 0 && given != 3) return CCQ_ERR_INVALID_ARG;
     if (given == 0 && p.t0 != 0) return CCQ_ERR_INVALID_ARG;
     if (dtype != CCQ_DTYPE_F32 && dtype != CCQ_DTYPE_BF16) return CCQ_ERR_UNSUPPORTED;
     if ((p.dk != 64 && p.dk != 128) || (p.dv != 64 && p.dv != 128)) return CCQ_ERR_UNSUPPORTED;
-    if (p.flags & ~(CCQ_FLAG_L2NORM_QK | CCQ_FLAG_FP32_PATH | CCQ_FLAG_TEST_STALL))
+    if (p.flags & ~(CCQ_FLAG_L2NORM_QK | CCQ_FLAG_FP32_PATH | CCQ_FLAG_PLAIN_GLA |
+                    CCQ_FLAG_TEST_STALL))
         return CCQ_ERR_INVALID_ARG;
     if ((long long)p.B * p.H > 0x7fffffffLL) return CCQ_ERR_UNSUPPORTED;
     if ((long long)p.T + p.t0 > (1LL << 40)) return CCQ_ERR_UNSUPPORTED;
@@ -104,14 +113,16 @@ extern "C" ccq_status ccq_gla_fwd(const void *q, const void *k, const void *v,
                 nullptr};
     ccq_status s = check_common(p, dtype);
     if (s != CCQ_OK) return s;
+    const bool bf16 = dtype == CCQ_DTYPE_BF16;
+    const bool tc = bf16 && !(flags & CCQ_FLAG_FP32_PATH) && tc_gla_supported(p);
+    // the test-only and measurement modes exist on the tensor-core kernel only
+    if ((flags & CCQ_FLAG_TEST_STALL) && !tc) return CCQ_ERR_UNSUPPORTED;
+    if ((flags & CCQ_FLAG_PLAIN_GLA) && (!tc || (flags & CCQ_FLAG_TEST_STALL)))
+        return CCQ_ERR_UNSUPPORTED;
     p.status = status_word();
     if (!p.status) return CCQ_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const bool bf16 = dtype == CCQ_DTYPE_BF16;
-    const bool tc = bf16 && !(flags & CCQ_FLAG_FP32_PATH) && tc_gla_supported(p);
-    if (flags & CCQ_FLAG_TEST_STALL) {
-        if (!tc) return CCQ_ERR_UNSUPPORTED;
-    }
+    if (flags & CCQ_FLAG_PLAIN_GLA) return to_status(launch_tc_gla_plain(p, st));
     if (tc) return to_status(launch_tc_gla(p, st));
     return to_status(launch_simt(p, false, bf16, st));
 }
@@ -130,7 +141,8 @@ extern "C" ccq_status ccq_gdn_fwd(const void *q, const void *k, const void *v,
     ccq_status s = check_common(p, dtype);
     if (s != CCQ_OK) return s;
     if (!beta && T > 0 && B > 0 && H > 0) return CCQ_ERR_INVALID_ARG;
-    if (flags & CCQ_FLAG_TEST_STALL) return CCQ_ERR_UNSUPPORTED;  // GLA tensor-core kernel only
+    if (flags & (CCQ_FLAG_TEST_STALL | CCQ_FLAG_PLAIN_GLA))  // GLA tensor-core kernel only
+        return CCQ_ERR_UNSUPPORTED;
     p.status = status_word();
     if (!p.status) return CCQ_ERR_CUDA;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -237,7 +237,10 @@ __device__ __forceinline__ void mma_k_loop(uint32_t d, uint64_t adesc, uint32_t 
 // cluster size set at launch).  QC = true: the covariance CTA alone (clusters
 // of one) writes the cleaned query qc itself (bf16, [B, H, T, dk]) to the
 // output tensor -- the first pass of the Gated DeltaNet forward.
-template <bool QC>
+// PLAIN = true (with QC = false): the plain GLA forward, lambda = 0 and no
+// key statistics -- CTA 0 only forms q * exp(-E) -- the baseline against
+// which the cost of the CCQ read is measured.
+template <bool QC, bool PLAIN = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
 tc_gla_kernel(const __grid_constant__ Args args) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -328,7 +331,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             auto prefetch = [&](int k) {
                 for (int b = 0; b < 2; ++b) {
                     tma_prefetch_3d(m0, b * 64, k * L, bh);
-                    tma_prefetch_3d(m1, b * 64, k * L, bh);
+                    if (!(PLAIN && rank == 0)) tma_prefetch_3d(m1, b * 64, k * L, bh);
                     if (!QC) tma_prefetch_3d(m2, b * 64, k * L, bh);
                 }
             };
@@ -344,11 +347,12 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 if (n >= 2 && !mbar_wait(smem_u32(&aux.empty[s]), ((n >> 1) - 1) & 1, abort)) break;
                 CCQ_TRACE(2, n, 0);
                 const uint32_t fb = smem_u32(&aux.full[s]);
-                mbar_expect_tx(fb, (rank == 0 && !QC ? 3 : 2) * TILE);
+                mbar_expect_tx(fb, (rank == 0 && !QC && !PLAIN ? 3 : 2) * TILE);
                 for (int b = 0; b < 2; ++b) {
                     tma_load_3d(smem_u32(smem + s * TILE + b * BOX), m0, fb, b * 64, n * L, bh);
-                    tma_load_3d(smem_u32(smem + base1 + s * stage1 + b * blk1), m1, fb, b * 64,
-                                n * L, bh);
+                    if (!(PLAIN && rank == 0))  // (the plain read needs no keys on CTA 0)
+                        tma_load_3d(smem_u32(smem + base1 + s * stage1 + b * blk1), m1, fb,
+                                    b * 64, n * L, bh);
                 }
                 uint32_t f2 = fb;
                 if (rank == 1) {
@@ -368,7 +372,19 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         // ============================================================ MMA issuer
         if (lane == 0) {
             const uint32_t sUX = smem_u32(smem + UXo);
-            if (rank == 0) {
+            if (rank == 0 && PLAIN) {
+                for (int n = 0; n < nch; ++n) {
+                    const int s = n & 1, b = n & 1;
+                    const uint32_t sLA = smem_u32(smem + CovLayout::LA + s * TILE);
+                    if (!mbar_wait(smem_u32(&aux.full[s]), (n >> 1) & 1, abort)) break;
+                    // the previous chunk's E^T has been read
+                    if (!mbar_wait(smem_u32(&aux.c0_ready), n & 1, abort)) break;
+                    tc_fence_after();
+                    mma_k_loop<true, false, 4>(tmem + E0_COL, sw128_desc(sLA, BOX, 1024), 0,
+                                               sw128_desc(sUX, 0, 1024), 0, ID_M128N64_MK, 0);
+                    mma_commit(smem_u32(&aux.p_full[b]));
+                }
+            } else if (rank == 0) {
                 for (int n = 0; n < nch; ++n) {
                     const int s = n & 1, b = n & 1;
                     const uint32_t ph2 = (n >> 1) & 1;
@@ -481,7 +497,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         // ============================================================ CTA 0 element-wise
         float m_cur;  // m[c] at the start of the current chunk
         bool fail = false;
-        const float b_lam = p.lambda_in ? 0.f : p.b_lambda[h];
+        const float b_lam = (PLAIN || p.lambda_in) ? 0.f : p.b_lambda[h];  // (no gate in plain mode)
 
         // ---- C accumulator := C0; chunk 0 operands (C0 snapshot, m / w dot rows)
         {
@@ -508,7 +524,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             m_cur = p.m0 ? p.m0[(size_t)bh * D + c] : 0.f;
             // dot rows of both K stages: w (hi, lo) and zero rows; m for chunk 0
             if (qt == 0) {
-                const float w = p.lambda_in ? 0.f : p.w_lambda[(size_t)h * D + c];
+                const float w = (PLAIN || p.lambda_in) ? 0.f : p.w_lambda[(size_t)h * D + c];
                 const float mh = __bfloat162float(__float2bfloat16_rn(m_cur));
                 const float wh = __bfloat162float(__float2bfloat16_rn(w));
                 put_bf16(smem + dot_off(0, 0, c), mh);
@@ -534,7 +550,54 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             }
         }
 
-        for (int n = 0; n < nch; ++n) {
+        // ---- plain GLA read: Qt = q * exp(-E), no key statistics
+        for (int n = 0; PLAIN && n < nch; ++n) {
+            const int b = n & 1;
+            const uint32_t ph2 = (n >> 1) & 1;
+            const bool more = n + 1 < nch;
+            if (tid == 0) bulk_wait_read1();  // send buffer b (chunk n-2) has been read
+            bool ok = wait_all(smem_u32(&aux.p_full[b]), ph2, abort) &&
+                      wait_all(smem_u32(&aux.full[b]), ph2, abort);
+            tc_fence_after();
+            if (epi_sync_any(!ok)) { fail = true; break; }
+            {
+                uint8_t *qtb = smem + CovLayout::QT + b * 16384;
+                const uint8_t *sQs = smem + CovLayout::Q + b * TILE;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    const int i0 = 16 * qt + 8 * g;
+                    uint32_t er[8];
+                    tmem_ld8(tl + E0_COL + i0, er);
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = bf16_at(sQs, i0 + e, c, 64);
+                    tmem_ld_wait();
+                    if (i0 == 0 && u2f(er[0]) < -80.f) record_status(p.status, CCQ_ERR_RANGE);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] *= exp2f(-1.4426950408889634f * u2f(er[e]));
+                    store8(qtb + sw128_chunk(c, i0, 128), v);
+                }
+            }
+            tc_fence_before();
+            fence_async_smem();
+            if (epi_sync_any(false)) { fail = true; break; }
+            if (tid == 0) {
+                if (more) mbar_arrive(smem_u32(&aux.c0_ready));  // E^T read
+                mbar_arrive(smem_u32(&aux.empty[b]));
+                bool sent = true;
+                if (n >= 2)
+                    sent = mbar_wait(smem_u32(&aux.qt_empty[b]), ((n >> 1) - 1) & 1, abort, true);
+                if (sent) {
+                    const uint32_t rfull = mapa(smem_u32(&aux.qt_full[b]), 1);
+                    const uint32_t rdst = mapa(smem_u32(smem + GlaLayout::QTR + b * 16384), 1);
+                    mbar_expect_tx_cluster(rfull, 16384);
+                    bulk_copy_to_peer(rdst, smem_u32(smem + CovLayout::QT + b * 16384), 16384,
+                                      rfull);
+                    bulk_commit();
+                }
+            }
+        }
+        for (int n = 0; !PLAIN && n < nch; ++n) {
             const int b = n & 1;
             const uint32_t ph2 = (n >> 1) & 1;
             const int c0t = n * L;
@@ -705,7 +768,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
             m_cur = m_next;
         }
         // ---- final state: C (TMEM accumulator), m
-        if (!fail && nch > 0) {
+        if (!PLAIN && !fail && nch > 0) {
             const bool ok = wait_all(smem_u32(&aux.p_full[(nch - 1) & 1]), ((nch - 1) >> 1) & 1, abort);
             tc_fence_after();
             if (ok && p.C_out) {
@@ -965,7 +1028,7 @@ bool tc_gla_supported(const CcqParams &p) {
            al(p.log_alpha) && al(p.o) && (long long)p.B * p.H * 2 < 0x7fffffffLL;
 }
 
-template <bool QC>
+template <bool QC, bool PLAIN>
 static cudaError_t launch_tc(const CcqParams &p, cudaStream_t st) {
     using namespace tcgla;
     Args a;
@@ -983,8 +1046,8 @@ static cudaError_t launch_tc(const CcqParams &p, cudaStream_t st) {
     static bool attr_set[64] = {};
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_set[dev]) {
-        e = cudaFuncSetAttribute(tc_gla_kernel<QC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SMEM_BYTES);
+        e = cudaFuncSetAttribute(tc_gla_kernel<QC, PLAIN>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
@@ -1001,13 +1064,22 @@ static cudaError_t launch_tc(const CcqParams &p, cudaStream_t st) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tc_gla_kernel<QC>, a);
+    return cudaLaunchKernelEx(&cfg, tc_gla_kernel<QC, PLAIN>, a);
 }
 
-cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st) { return launch_tc<false>(p, st); }
+cudaError_t launch_tc_gla(const CcqParams &p, cudaStream_t st) {
+    return launch_tc<false, false>(p, st);
+}
+
+// The plain GLA forward (lambda = 0, no key statistics) on the same pipeline.
+cudaError_t launch_tc_gla_plain(const CcqParams &p, cudaStream_t st) {
+    return launch_tc<false, true>(p, st);
+}
 
 // First pass of the tensor-core Gated DeltaNet forward: qc (bf16) into p.o,
 // plus lambda_out, C_out and m_out.
-cudaError_t launch_tc_qclean(const CcqParams &p, cudaStream_t st) { return launch_tc<true>(p, st); }
+cudaError_t launch_tc_qclean(const CcqParams &p, cudaStream_t st) {
+    return launch_tc<true, false>(p, st);
+}
 
 }  // namespace ccq

@@ -82,6 +82,13 @@ typedef enum { CCQ_DTYPE_F32 = 0, CCQ_DTYPE_BF16 = 1 } ccq_dtype;
 
 #define CCQ_FLAG_L2NORM_QK 1u  /* normalise q and k by 1/sqrt(|x|^2 + 1e-6) before use */
 #define CCQ_FLAG_FP32_PATH 2u  /* force the fp32 CUDA-core kernel (any dtype/shape) */
+/* Measurement baseline: the plain GLA forward, o_t = S_t^T q_t (lambda = 0)
+ * with no key statistics, on the same tensor-core pipeline -- the cost of the
+ * CCQ read is the difference.  ccq_gla_fwd only, bf16 with dk = dv = 128 and
+ * T > 0 (else CCQ_ERR_UNSUPPORTED); C0, m0, C_out, m_out, lambda_in and
+ * lambda_out must be NULL, w_lambda / b_lambda are ignored, S0 / S_out as
+ * usual (else CCQ_ERR_INVALID_ARG). */
+#define CCQ_FLAG_PLAIN_GLA 4u
 /* Test only (failure detection): the tensor-core kernel issues no input loads,
  * so its bounded waits run out after a few seconds and the call records
  * CCQ_ERR_TIMEOUT without faulting or hanging the GPU.  Requires a shape the

@@ -130,3 +130,20 @@ def test_gdn_step_requires_beta(lib):
 def test_step_empty_batch_needs_no_pointers(lib):
     none = dict(q=None, k=None, v=None, la=None, o=None, S=None, C=None, m=None, w=None, b=None)
     assert _step(lib, B=0, **none) == 0
+
+
+@pytest.mark.parametrize("case,code", [
+    (dict(flags=ccq.FLAG_PLAIN_GLA, S0=FAKE, C0=FAKE, m0=FAKE, t0=3), 1),  # no statistics
+    (dict(flags=ccq.FLAG_PLAIN_GLA, lout=FAKE), 1),
+    (dict(flags=ccq.FLAG_PLAIN_GLA, lin=FAKE), 1),
+    (dict(flags=ccq.FLAG_PLAIN_GLA), 2),                       # fp32, d64: not a tensor-core shape
+    (dict(flags=ccq.FLAG_PLAIN_GLA, dtype=1, dk=128, dv=128, T=0), 2),
+])
+def test_plain_gla_flag_checked_synchronously(lib, case, code):
+    assert _gla(lib, **case) == code
+
+
+def test_gdn_refuses_the_plain_flag(lib):
+    assert lib.ccq_gdn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None, None,
+                           None, 0, None, None, None, 1, 1, 8, 128, 128, 0, 1,
+                           ccq.FLAG_PLAIN_GLA, None) == 2

@@ -204,3 +204,40 @@ def test_fp32_path_flag_on_bf16_matches_oracle():
     inp = _small("gla", "bf16", 128, 128, 200, B=1, H=2, seed=13)
     gpu, ref = run_both("gla", inp, "bf16", flags=ccq.FLAG_FP32_PATH)
     check_all(gpu, ref, "bf16", "fp32 path")
+
+
+# ----------------------------------------------------------------- plain GLA baseline
+@pytest.mark.parametrize("T", [64, 200, 4096])
+def test_plain_gla_baseline_is_the_lambda_zero_read(T):
+    """CCQ_FLAG_PLAIN_GLA computes the backbone's own read o_t = S_t^T q_t:
+    the oracle with lambda = 0 gives it exactly (q_clean = q)."""
+    inp = _small("gla", "bf16", 128, 128, T, B=1, H=4, seed=30 + T, keys="aniso")
+    d = to_dev(inp)
+    rng = np.random.default_rng(T)
+    S0 = (rng.standard_normal((1, 4, 128, 128)) * 0.1).astype(np.float32)
+    o, st = ccq.gla_fwd(d["q"], d["k"], d["v"], d["log_alpha"], flags=ccq.FLAG_PLAIN_GLA,
+                        S0=torch.from_numpy(S0).cuda())
+    torch.cuda.synchronize()
+    assert ccq.last_device_status() == 0
+    assert st["C"] is None and st["m"] is None
+    lin = np.zeros((1, 4, T), np.float32)
+    C0 = np.zeros((1, 4, 128, 128), np.float32)
+    m0 = np.zeros((1, 4, 128), np.float32)
+    ref = oracle.run("gla", inp["q"], inp["k"], inp["v"], inp["log_alpha"], lambda_in=lin,
+                     S0=S0, C0=C0, m0=m0)
+    check(np64(o), ref["o"], "bf16", f"plain T={T} o")
+    check(np64(st["S"]), ref["S"], "bf16", f"plain T={T} S", per_head=False)
+
+
+def test_plain_gla_flag_refuses_statistics_and_other_paths():
+    inp = _small("gla", "bf16", 128, 128, 64, B=1, H=2, seed=3)
+    d = to_dev(inp)
+    with pytest.raises(ccq.CcqError) as e:  # lambda_out is a statistic of the CCQ read
+        ccq.gla_fwd(d["q"], d["k"], d["v"], d["log_alpha"], flags=ccq.FLAG_PLAIN_GLA,
+                    lambda_out=torch.empty((1, 2, 64), device="cuda"))
+    assert e.value.code == 1
+    inp32 = _small("gla", "f32", 64, 64, 64, B=1, H=2, seed=3)
+    d32 = to_dev(inp32)
+    with pytest.raises(ccq.CcqError) as e:  # tensor-core shapes only
+        ccq.gla_fwd(d32["q"], d32["k"], d32["v"], d32["log_alpha"], flags=ccq.FLAG_PLAIN_GLA)
+    assert e.value.code == 2
