@@ -66,10 +66,11 @@ struct Smem {
     __nv_bfloat16 St[W][DKP];    // bf16 copy of the S slice, transposed ([column][row])
     __nv_bfloat16 Ut[W][L];      // bf16 U, transposed
     float V[L][W];
-    float la[L], beta[L];
-    float Aw[L][L], Ag[L][L];
+    // per-token scalars, by chunk parity: beta, g, exp(g), exp(-g), exp(g_L - g)
+    float beta[2][L], G[2][L], E[2][L], EI[2][L], Dd[2][L];
+    __align__(16) float AwT[L][L];                 // Aw transposed: [column][row]
+    float Ag[L][L];
     float X[L][W], QS[L][W], U[L][W];
-    float G[L], E[L], Dd[L];
 };
 
 // One chunk's inputs as loaded by one thread: 16 bytes of a K row and of a qc
@@ -105,12 +106,34 @@ gdn_rule_kernel(const __grid_constant__ CcqParams p) {
         Chunk x;
         x.k = *reinterpret_cast<const uint4 *>(gk + row * DK + 8 * part);
         x.q = *reinterpret_cast<const uint4 *>(go + row * DV + 8 * part);
-        const int i = min(tid / W, last), j = tid % W, t = min(tid & (L - 1), last);
+        const int i = min(tid / W, last), j = tid % W, t = min(lane & (L - 1), last);
         x.v = gv[(size_t)(c * L + i) * DV + j0 + j];
         x.la = gla[c * L + t];
         x.beta = gbeta[c * L + t];
         return x;
     };
+    // warp 1 (which holds chunk c's log alphas) forms the cumulative
+    // log-decay g, exp(+-g), exp(g_L - g) and beta into the chunk's parity slot
+    // (|g| over a chunk stays far from the fp32 exponent range, so
+    // Gam_il = exp(g_i) exp(-g_l) is formed by one product)
+    auto scan = [&](const Chunk &x, int c) {
+        const int lc = min(L, T - c * L), pb = c & 1;
+        float g = (lane < L && lane < lc) ? __bfloat162float(x.la) : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, g, o);
+            if (lane >= o) g += y;
+        }
+        const float gL = __shfl_sync(0xffffffffu, g, L - 1);
+        if (lane < L) {
+            sm.beta[pb][lane] = lane < lc ? __bfloat162float(x.beta) : 0.f;
+            sm.G[pb][lane] = g;
+            sm.E[pb][lane] = expf(g);
+            sm.EI[pb][lane] = expf(-g);
+            sm.Dd[pb][lane] = expf(gL - g);
+        }
+    };
+    // stores a fetched chunk's tiles
     auto store = [&](const Chunk &x, int c) {
         const int lc = min(L, T - c * L);
         const int r = tid >> 4, part = tid & 15;
@@ -118,10 +141,6 @@ gdn_rule_kernel(const __grid_constant__ CcqParams p) {
         *reinterpret_cast<uint4 *>(&sm.K[r][8 * part]) = r < lc ? x.k : z;
         *reinterpret_cast<uint4 *>(&sm.Q[r][8 * part]) = r < lc ? x.q : z;
         sm.V[tid / W][tid % W] = tid / W < lc ? __bfloat162float(x.v) : 0.f;
-        if (tid < L) {
-            sm.la[tid] = tid < lc ? __bfloat162float(x.la) : 0.f;
-            sm.beta[tid] = tid < lc ? __bfloat162float(x.beta) : 0.f;
-        }
     };
 
     // ---- S slice: warp w holds rows [16w, 16w+16) x 16 columns as two m16n8
@@ -138,7 +157,11 @@ gdn_rule_kernel(const __grid_constant__ CcqParams p) {
                 sm.St[j][r] = __float2bfloat16_rn(sacc[nt][e]);
             }
     }
-    if (nch > 0) store(fetch(0), 0);
+    if (nch > 0) {
+        const Chunk x0 = fetch(0);
+        store(x0, 0);
+        if (warp == 1) scan(x0, 0);
+    }
     __syncthreads();
     // this CTA holds chunk 0's qc; o may overwrite a chunk's qc once every CTA
     // of the cluster has said so (each wait sits just before the chunk's first
@@ -151,22 +174,8 @@ gdn_rule_kernel(const __grid_constant__ CcqParams p) {
         Chunk nxt{};
         if (c + 1 < nch) nxt = fetch(c + 1);
 
-        // ---- cumulative log-decay of the chunk (one warp, shuffle scan)
-        if (warp == 0) {
-            float g = lane < L ? sm.la[lane] : 0.f;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, g, o);
-                if (lane >= o) g += y;
-            }
-            if (lane < L) sm.G[lane] = g;
-        }
-        __syncthreads();
-        const float gL = sm.G[L - 1];
-        if (tid < L) {
-            sm.E[tid] = expf(sm.G[tid]);
-            sm.Dd[tid] = expf(gL - sm.G[tid]);
-        }
+        const int pb = c & 1;  // parity slot of this chunk's per-token scalars
+        const float gL = sm.G[pb][L - 1];
 
         // ---- four 16 x 8 tiles per product over k = 128: warp (prod, nt)
         {
@@ -191,13 +200,13 @@ gdn_rule_kernel(const __grid_constant__ CcqParams p) {
             for (int e = 0; e < 4; ++e) {
                 const int i = g4 + 8 * (e >> 1), n = 8 * nt + 2 * t4 + (e & 1);
                 const bool row_ok = i < lc;
+                const float gam = sm.E[pb][i] * sm.EI[pb][n];
                 if (prod == 0) {
-                    sm.Aw[i][n] = (row_ok && n < i)
-                                      ? sm.beta[i] * expf(sm.G[i] - sm.G[n]) * d[e] : 0.f;
+                    sm.AwT[n][i] = (row_ok && n < i) ? sm.beta[pb][i] * gam * d[e] : 0.f;
                 } else if (prod == 1) {
-                    sm.Ag[i][n] = (row_ok && n <= i) ? expf(sm.G[i] - sm.G[n]) * d[e] : 0.f;
+                    sm.Ag[i][n] = (row_ok && n <= i) ? gam * d[e] : 0.f;
                 } else if (prod == 2) {
-                    sm.X[i][n] = row_ok ? sm.beta[i] * (sm.V[i][n] - expf(sm.G[i]) * d[e]) : 0.f;
+                    sm.X[i][n] = row_ok ? sm.beta[pb][i] * (sm.V[i][n] - sm.E[pb][i] * d[e]) : 0.f;
                 } else {
                     sm.QS[i][n] = d[e];
                 }
@@ -205,20 +214,35 @@ gdn_rule_kernel(const __grid_constant__ CcqParams p) {
         }
         __syncthreads();
 
-        // ---- U = (I + Aw)^-1 X: lane j of warp 0 walks column j down the rows
+        // ---- U = (I + Aw)^-1 X: lane j of warp 0 owns column j; right-looking
+        // elimination (once u_l is final, every later row subtracts its share:
+        // independent updates, so the dependent depth is one FMA per row)
         if (warp == 0 && lane < W) {
             const int j = lane;
             float u[L];
 #pragma unroll
-            for (int i = 0; i < L; ++i) {
-                float x = sm.X[i][j];
+            for (int i = 0; i < L; ++i) u[i] = sm.X[i][j];
 #pragma unroll
-                for (int l = 0; l < i; ++l) x -= sm.Aw[i][l] * u[l];
-                u[i] = x;
-                sm.U[i][j] = x;
-                sm.Ut[j][i] = __float2bfloat16_rn(x);
+            for (int l = 0; l < L - 1; ++l) {
+                float a[L];  // column l of Aw (same address in every lane)
+#pragma unroll
+                for (int q = (l + 1) / 4; q < L / 4; ++q) {
+                    const float4 f = reinterpret_cast<const float4 *>(&sm.AwT[l][0])[q];
+                    a[4 * q] = f.x;
+                    a[4 * q + 1] = f.y;
+                    a[4 * q + 2] = f.z;
+                    a[4 * q + 3] = f.w;
+                }
+#pragma unroll
+                for (int i = l + 1; i < L; ++i) u[i] -= a[i] * u[l];
+            }
+#pragma unroll
+            for (int i = 0; i < L; ++i) {
+                sm.U[i][j] = u[i];
+                sm.Ut[j][i] = __float2bfloat16_rn(u[i]);
             }
         }
+        if (warp == 1 && c + 1 < nch) scan(nxt, c + 1);  // next chunk's scalars, meanwhile
         __syncthreads();
 
         // ---- O = exp(g) QS + Ag U (fp32, one (i, j) per thread)
@@ -226,7 +250,7 @@ gdn_rule_kernel(const __grid_constant__ CcqParams p) {
         {
             const int i = tid / W, j = tid % W;
             if (i < lc) {
-                float a = sm.E[i] * sm.QS[i][j];
+                float a = sm.E[pb][i] * sm.QS[i][j];
 #pragma unroll
                 for (int l = 0; l < L; ++l) a += sm.Ag[i][l] * sm.U[l][j];
                 go[(size_t)(c0 + i) * DV + j0 + j] = __float2bfloat16_rn(a);
@@ -241,8 +265,8 @@ gdn_rule_kernel(const __grid_constant__ CcqParams p) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int m = g4 + 8 * (q & 1), k = 2 * t4 + 8 * (q >> 1);
-                a[q] = pack_bf16(bf(&sm.K[k][r0 + m]) * sm.Dd[k],
-                                 bf(&sm.K[k + 1][r0 + m]) * sm.Dd[k + 1]);
+                a[q] = pack_bf16(bf(&sm.K[k][r0 + m]) * sm.Dd[pb][k],
+                                 bf(&sm.K[k + 1][r0 + m]) * sm.Dd[pb][k + 1]);
             }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
