@@ -2,7 +2,7 @@
 fp32 state) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gla_fwd|gdn_fwd|gla_step|gdn_step|ccq_overhead]
+                    [--workload gla_fwd|gdn_fwd|gla_step|gdn_step|ccq_overhead|sigma_subspace]
 
 Default (the headline): one step = one CCQ-GLA forward over the whole batch
 (read + gate + stats + GLA write/read, final state written).  The other
@@ -426,6 +426,61 @@ def run_overhead(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_subspace(args, world, rank, local):
+    """Top-16 eigenspace of Sigma_T for the 64 heads of the benchmark workload's
+    final state (after its T4096 forward), 100 orthogonal iterations, and the
+    captured energy of all 262,144 keys: the key-geometry diagnostic."""
+    import ccq_read_side_gb300 as ccq
+    from ccq_read_side_gb300.workloads import WORKLOADS, make_inputs
+
+    w = WORKLOADS[WORKLOAD_INDEX]
+    inp = make_inputs(w)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    _, st = ccq.gla_fwd(d["q"], d["k"], d["v"], d["log_alpha"], d["w_lambda"], d["b_lambda"])
+    C, m, n, k, iters = st["C"], st["m"], w.T, 16, 100
+    stream = torch.cuda.current_stream()
+
+    def step():
+        U, _ = ccq.sigma_subspace(C, m, n, k=k, iters=iters, stream=stream)
+        ccq.subspace_alignment(U, d["k"], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) * 1e-3 / args.steps
+    BH, dk = w.B * w.H, w.dk
+    # fp32 FLOPs: per iteration Sigma V (2 dk^2 k) and the Cholesky-QR (2 dk k^2 twice),
+    # plus the alignment (2 dk k per key)
+    flops = BH * iters * (2 * dk * dk * k + 4 * dk * k * k) + 2 * dk * k * BH * w.T
+    fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12  # TFLOP/s: SMs x FP32 lanes x FMA x max clock
+    if rank != 0:
+        return
+    line = {
+        "metric": "CCQ key-geometry diagnostic: top-16 eigenspace of Sigma_T per head + key "
+                  "alignment, B4 H16 T4096 d128, 1xGB300",
+        "value": BH / t, "unit": "heads/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name + "_sigma_top16", "heads": BH, "dk": dk, "k": k,
+                   "iters": iters, "keys": BH * w.T, "l2": "state and keys L2-resident "
+                   "(diagnostic; 66 MB)"},
+        "roofline": {"bound": "alu", "achieved": flops / t / 1e12, "peak": fp32_peak,
+                     "unit": "TFLOP/s", "frac": flops / t / 1e12 / fp32_peak,
+                     "peak_source": "152 SMs x 128 fp32 lanes x 2 x 2.07 GHz (nominal)"},
+        "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def ccq_launches_per_step() -> int:
     return 1  # one fused kernel launch per forward (or per decode step)
 
@@ -583,7 +638,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["gla_fwd", "gdn_fwd", "gla_step", "gdn_step",
-                                           "ccq_overhead"], default="gla_fwd")
+                                           "ccq_overhead", "sigma_subspace"],
+                    default="gla_fwd")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -595,6 +651,8 @@ def main():
             run_step(args, world, rank, local)
         elif args.workload == "ccq_overhead":
             run_overhead(args, world, rank, local)
+        elif args.workload == "sigma_subspace":
+            run_subspace(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

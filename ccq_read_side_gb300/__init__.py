@@ -16,7 +16,8 @@ from typing import Dict, Optional, Tuple
 
 import torch
 
-__all__ = ["gla_fwd", "gdn_fwd", "gla_step", "gdn_step", "last_device_status", "status_string", "CcqError",
+__all__ = ["gla_fwd", "gdn_fwd", "gla_step", "gdn_step", "sigma_subspace",
+           "subspace_alignment", "last_device_status", "status_string", "CcqError",
            "library", "FLAG_L2NORM_QK", "FLAG_FP32_PATH", "FLAG_PLAIN_GLA", "FLAG_TEST_STALL",
            "STATUS"]
 
@@ -60,6 +61,10 @@ def library() -> ctypes.CDLL:
     lib.ccq_gla_step.argtypes = [P, P, P, P, P, P] + step_tail
     lib.ccq_gdn_step.restype = I
     lib.ccq_gdn_step.argtypes = [P, P, P, P, P, P, P] + step_tail
+    lib.ccq_sigma_subspace.restype = I
+    lib.ccq_sigma_subspace.argtypes = [P, P, ctypes.c_int64, I, I, I, I, P, P, P]
+    lib.ccq_subspace_alignment.restype = I
+    lib.ccq_subspace_alignment.argtypes = [P, P, I, I, I, I, I, P, P]
     lib.ccq_status_string.restype = ctypes.c_char_p
     lib.ccq_status_string.argtypes = [I]
     lib.ccq_last_device_status.restype = I
@@ -224,3 +229,45 @@ def gdn_step(q, k, v, log_alpha, beta, S, C, m, t0: int, w_lambda=None, b_lambda
     """One decode step on the Gated DeltaNet backbone (log_alpha, beta [B,H])."""
     return _step("gdn", q, k, v, log_alpha, beta, w_lambda, b_lambda, lambda_in, S, C, m, t0,
                  o, lambda_out, flags, stream)
+
+
+def sigma_subspace(C, m, n: int, k: int = 16, iters: int = 100, stream=None):
+    """Top-k eigenspace of Sigma = C/n - mu mu^T per head from a final state
+    (C [..., dk, dk], m [..., dk] fp32 CUDA tensors).  Returns (U [..., dk, k]
+    orthonormal Ritz vectors, ritz [..., k] values, descending)."""
+    dk = C.shape[-1]
+    lead = tuple(C.shape[:-2])
+    BH = 1
+    for s_ in lead:
+        BH *= s_
+    _need(C, "C", torch.float32, lead + (dk, dk))
+    _need(m, "m", torch.float32, lead + (dk,), C.device)
+    U = torch.empty(lead + (dk, k), dtype=torch.float32, device=C.device)
+    ritz = torch.empty(lead + (k,), dtype=torch.float32, device=C.device)
+    with torch.cuda.device(C.device):
+        rc = library().ccq_sigma_subspace(_ptr(C), _ptr(m), int(n), BH, dk, int(k), int(iters),
+                                          _ptr(U), _ptr(ritz), _stream(stream))
+    if rc != 0:
+        raise CcqError(rc, "ccq_sigma_subspace")
+    return U, ritz
+
+
+def subspace_alignment(U, X, stream=None):
+    """|U^T x|^2 / |x|^2 for every key x in X [..., nx, dk] (U [..., dk, k])."""
+    dk, k = U.shape[-2:]
+    lead = tuple(U.shape[:-2])
+    BH = 1
+    for s_ in lead:
+        BH *= s_
+    nx = X.shape[-2]
+    if X.dtype not in _DTYPES:
+        raise ValueError(f"unsupported dtype {X.dtype}")
+    _need(U, "U", torch.float32, lead + (dk, k))
+    _need(X, "X", X.dtype, lead + (nx, dk), U.device)
+    out = torch.empty(lead + (nx,), dtype=torch.float32, device=U.device)
+    with torch.cuda.device(U.device):
+        rc = library().ccq_subspace_alignment(_ptr(U), _ptr(X), BH, dk, k, nx, _DTYPES[X.dtype],
+                                              _ptr(out), _stream(stream))
+    if rc != 0:
+        raise CcqError(rc, "ccq_subspace_alignment")
+    return out

@@ -92,6 +92,12 @@ static ccq_status check_step(const void *q, const void *k, const void *v,
     return CCQ_OK;
 }
 
+// Key-covariance diagnostics (subspace.cu).
+cudaError_t launch_sigma_subspace(const float *C, const float *m, double n, int BH, int dk, int k,
+                                  int iters, float *U, float *ritz, cudaStream_t st);
+cudaError_t launch_alignment(const float *U, const void *X, bool bf16, int BH, int dk, int k,
+                             int nx, float *align, cudaStream_t st);
+
 static ccq_status to_status(cudaError_t e) {
     if (e == cudaSuccess) return CCQ_OK;
     return CCQ_ERR_CUDA;
@@ -190,6 +196,29 @@ extern "C" ccq_status ccq_gdn_step(const void *q, const void *k, const void *v,
                                  lambda_out, o, S, C, m, (long long)t0, B, H, dk, dv, true,
                                  dtype == CCQ_DTYPE_BF16, flags, st_word,
                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" ccq_status ccq_sigma_subspace(const float *C, const float *m, int64_t n, int BH, int dk,
+                                         int k, int iters, float *U, float *ritz,
+                                         ccq_stream_t stream) {
+    if (BH < 0 || n < 1 || k < 1 || iters < 0 || iters > 100000) return CCQ_ERR_INVALID_ARG;
+    if ((dk != 64 && dk != 128) || k > 32 || k > dk) return CCQ_ERR_UNSUPPORTED;
+    if (BH == 0) return CCQ_OK;
+    if (!C || !m || !U || !ritz) return CCQ_ERR_INVALID_ARG;
+    return to_status(launch_sigma_subspace(C, m, (double)n, BH, dk, k, iters, U, ritz,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" ccq_status ccq_subspace_alignment(const float *U, const void *X, int BH, int dk, int k,
+                                             int nx, ccq_dtype dtype, float *align,
+                                             ccq_stream_t stream) {
+    if (BH < 0 || nx < 0 || k < 1 || dk < 1) return CCQ_ERR_INVALID_ARG;
+    if (dtype != CCQ_DTYPE_F32 && dtype != CCQ_DTYPE_BF16) return CCQ_ERR_UNSUPPORTED;
+    if ((long long)BH * nx * 32 > 0x7fffffffLL || k > dk) return CCQ_ERR_UNSUPPORTED;
+    if ((long long)BH * nx == 0) return CCQ_OK;
+    if (!U || !X || !align) return CCQ_ERR_INVALID_ARG;
+    return to_status(launch_alignment(U, X, dtype == CCQ_DTYPE_BF16, BH, dk, k, nx, align,
+                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 extern "C" const char *ccq_status_string(ccq_status s) {

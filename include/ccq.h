@@ -154,6 +154,30 @@ ccq_status ccq_gdn_step(const void *q, const void *k, const void *v, const void 
                         float *m, int64_t t0, int B, int H, int dk, int dv, ccq_dtype dtype,
                         unsigned flags, ccq_stream_t stream);
 
+/*
+ * Geometry of the key statistics (the article's diagnosis, 10100.com
+ * "method": keys concentrate in a few dominant directions and a needle that
+ * lies off them is what the plain read loses).  For each of BH heads, from a
+ * final state C [BH, dk, dk] and m [BH, dk] (float32) after n >= 1 tokens:
+ * the top-k invariant subspace of Sigma = C/n - mu mu^T (mu = m/n) by
+ * orthogonal iteration (`iters` steps of Sigma V, Cholesky-QR) and a
+ * Rayleigh-Ritz step.  U [BH, dk, k]: orthonormal Ritz vectors (column a of
+ * head bh at U[bh][i][a]); ritz [BH, k]: Ritz values, descending.  dk in
+ * {64, 128}, 1 <= k <= 32.  Convergence needs a gap between the k-th and
+ * (k+1)-th eigenvalue; iters ~ 50-100 suffices for a ratio below 0.8.
+ * Asynchronous on `stream`; float32 arithmetic; the library allocates nothing.
+ */
+ccq_status ccq_sigma_subspace(const float *C, const float *m, int64_t n, int BH, int dk, int k,
+                              int iters, float *U, float *ritz, ccq_stream_t stream);
+
+/*
+ * Captured energy of keys in a subspace: align[bh][j] = |U_bh^T x|^2 / |x|^2
+ * for x = X[bh][j][:] (X [BH, nx, dk] in `dtype`, U as ccq_sigma_subspace
+ * writes it).  A zero key gives 0.
+ */
+ccq_status ccq_subspace_alignment(const float *U, const void *X, int BH, int dk, int k, int nx,
+                                  ccq_dtype dtype, float *align, ccq_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char *ccq_status_string(ccq_status s);
 

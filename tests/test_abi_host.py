@@ -147,3 +147,16 @@ def test_gdn_refuses_the_plain_flag(lib):
     assert lib.ccq_gdn_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, FAKE, None, None,
                            None, 0, None, None, None, 1, 1, 8, 128, 128, 0, 1,
                            ccq.FLAG_PLAIN_GLA, None) == 2
+
+
+def test_subspace_diagnostics_validate_synchronously(lib):
+    # k above 32 / above dk -> unsupported; n < 1 or missing pointers -> invalid;
+    # an empty batch needs no pointers and makes no CUDA call
+    assert lib.ccq_sigma_subspace(FAKE, FAKE, 10, 1, 128, 33, 10, FAKE, FAKE, None) == 2
+    assert lib.ccq_sigma_subspace(FAKE, FAKE, 10, 1, 96, 4, 10, FAKE, FAKE, None) == 2
+    assert lib.ccq_sigma_subspace(FAKE, FAKE, 0, 1, 128, 4, 10, FAKE, FAKE, None) == 1
+    assert lib.ccq_sigma_subspace(None, FAKE, 10, 1, 128, 4, 10, FAKE, FAKE, None) == 1
+    assert lib.ccq_sigma_subspace(None, None, 10, 0, 128, 4, 10, None, None, None) == 0
+    assert lib.ccq_subspace_alignment(FAKE, FAKE, 1, 128, 16, 4, 7, FAKE, None) == 2
+    assert lib.ccq_subspace_alignment(None, FAKE, 1, 128, 16, 4, 1, FAKE, None) == 1
+    assert lib.ccq_subspace_alignment(None, None, 0, 128, 16, 4, 1, None, None) == 0
