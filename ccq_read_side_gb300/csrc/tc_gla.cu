@@ -108,7 +108,7 @@ __host__ __device__ constexpr uint32_t dot_off(int s, int row, int c) {
 struct Aux {
     uint64_t full[2], empty[2];  // TMA stages (CTA 1: K and log alpha; V below)
     uint64_t vfull[2];           // CTA 1: V tile of a stage
-    uint64_t aqk_full, p_full[2], m_ready, c0_ready, ahat_ready, qt_empty[2];  // CTA 0
+    uint64_t aqk_full, p_full[2], c_full, m_ready, c0_ready, ahat_ready, qt_empty[2];  // CTA 0
     uint64_t qt_full[2], kh_ready, sb_ready, ds_full, stage1, ek_full, ag_ready, o_full[2];  // CTA 1
     uint32_t tmem_base;
     int abort;
@@ -276,6 +276,7 @@ tc_gla_kernel(const __grid_constant__ Args args) {
         mbar_init(smem_u32(&aux.c0_ready), 1);
         mbar_init(smem_u32(&aux.ahat_ready), 1);
         mbar_init(smem_u32(&aux.m_ready), 1);
+        mbar_init(smem_u32(&aux.c_full), 1);
         mbar_init(smem_u32(&aux.kh_ready), 1);
         mbar_init(smem_u32(&aux.sb_ready), 1);
         mbar_init(smem_u32(&aux.ds_full), 1);
@@ -420,6 +421,8 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     if (!QC)
                         mma_k_loop<true, false, 4>(tmem + E0_COL, sw128_desc(sLA, BOX, 1024), 0,
                                                    sw128_desc(sUX, 0, 1024), 0, ID_M128N64_MK, 0);
+                    // C is final for this chunk: the query phase snapshots it first
+                    mma_commit(smem_u32(&aux.c_full));
                     CCQ_TRACE(1, n, 8);
                     if (!mbar_wait(smem_u32(&aux.ahat_ready), n & 1, abort)) break;
                     tc_fence_after();
@@ -459,15 +462,17 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                         // E^T of chunk n has been read: the next chunk's E^T may
                         // overwrite it while the element-wise warps build Sb
                         if (n + 1 < nch && !issue_ek(n + 1)) break;
-                        if (!mbar_wait(smem_u32(&aux.sb_ready), n & 1, abort)) break;
                         CCQ_TRACE(1, n, 0);
                         if (!mbar_wait(smem_u32(&aux.qt_full[b]), ph2, abort, true)) break;
                         tc_fence_after();
                         CCQ_TRACE(1, n, 1);
-                        // Ag = Qt Kh^T (channel-major operands)
+                        // Ag = Qt Kh^T (channel-major operands): needs no Sb, so it
+                        // runs while the element-wise warps still build the snapshot
                         mma_k_loop<true, true, 8>(tmem + AG_COL, sw128_desc(sQT, 16384, 1024), 0,
                                                sw128_desc(sKH, 16384, 1024), 0, ID_M64N64_MM, 0);
                         CCQ_TRACE(1, n, 6);
+                        if (!mbar_wait(smem_u32(&aux.sb_ready), n & 1, abort)) break;
+                        tc_fence_after();
                         // O^T = Sb^T Qt^T
                         mma_k_loop<true, true, 8>(tmem + O_COL(b), sw128_desc(sSB, 16384, 1024), 0,
                                                sw128_desc(sQT, 16384, 1024), 0, ID_M128N64_MM, 0);
@@ -683,9 +688,28 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                 CCQ_TRACE(0, n, 4);
             }
 
-            // ---- cleaned, decay-scaled query Qt^T (thread = channel c, 16 tokens),
-            //      then the next chunk's C0 snapshot (C after this chunk's update)
-            ok = wait_all(smem_u32(&aux.p_full[b]), ph2, abort);
+            // ---- the next chunk's C0 snapshot (C after this chunk's update, final
+            //      before the last MMA group), then the cleaned, decay-scaled
+            //      query Qt^T (thread = channel c, 16 tokens)
+            ok = wait_all(smem_u32(&aux.c_full), n & 1, abort);
+            tc_fence_after();
+            if (ok && more) {
+                uint8_t *c0n = smem + CovLayout::C0 + (b ^ 1) * 32768;
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb) {
+                    uint32_t cr[16];
+                    tmem_ld16(tl + C_COL + 32 * qt + 16 * hb, cr);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int g = 0; g < 2; ++g) {
+                        float v[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = u2f(cr[8 * g + e]);
+                        store8(c0n + sw128_chunk(c, 32 * qt + 16 * hb + 8 * g, 128), v);
+                    }
+                }
+            }
+            ok = ok && wait_all(smem_u32(&aux.p_full[b]), ph2, abort);
             tc_fence_after();
             if (tid == 0) CCQ_TRACE(0, n, 8);
             if (ok) {
@@ -721,22 +745,6 @@ tc_gla_kernel(const __grid_constant__ Args args) {
                     }
                 }
                 if (tid == 0) CCQ_TRACE(2, n, 5);
-                if (more) {
-                    uint8_t *c0n = smem + CovLayout::C0 + (b ^ 1) * 32768;
-#pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        uint32_t cr[16];
-                        tmem_ld16(tl + C_COL + 32 * qt + 16 * hb, cr);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int g = 0; g < 2; ++g) {
-                            float v[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) v[e] = u2f(cr[8 * g + e]);
-                            store8(c0n + sw128_chunk(c, 32 * qt + 16 * hb + 8 * g, 128), v);
-                        }
-                    }
-                }
             }
             if (tid == 0) CCQ_TRACE(2, n, 4);
             tc_fence_before();
