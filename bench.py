@@ -292,8 +292,23 @@ def run_ours(args, world, rank, local):
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
     d2h = o_host.numel() * o_host.element_size()
 
+    # each input's copy on its own stream (several copy engines at once); the
+    # copies of a step start after the previous step's work has been enqueued
+    # and the forward waits for all of them
+    side = [torch.cuda.Stream(device=dev) for _ in keys]
+    dbuf = {k: torch.empty(host[k].shape, dtype=host[k].dtype, device=dev) for k in keys}
+
     def e2e_step():
-        dd = {k: host[k].to(dev, non_blocking=True) for k in keys}
+        start = torch.cuda.Event()
+        start.record(stream)
+        for s_, k in zip(side, keys):
+            s_.wait_event(start)
+            with torch.cuda.stream(s_):
+                dbuf[k].copy_(host[k], non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(s_)
+            stream.wait_event(done)
+        dd = dbuf
         if gdn:
             oo, _ = ccq.gdn_fwd(dd["q"], dd["k"], dd["v"], dd["log_alpha"], dd["beta"],
                                 dd["w_lambda"], dd["b_lambda"], want_state=False, stream=stream)
