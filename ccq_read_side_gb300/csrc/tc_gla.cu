@@ -27,9 +27,10 @@
 //   colsum(K), which advances m, is summed by the element-wise threads from
 //   the K tile while they wait for A.
 //
-//   Per chunk CTA 0 has three element-wise phases and two MMA commits: the
-//   m rows for the next chunk's Q K^T are ready after the gate phase, the
-//   next C0 snapshot after the query phase.
+//   Per chunk CTA 0 has three element-wise phases and three MMA commits: the
+//   m rows for the next chunk's Q K^T are ready after the gate phase, the next
+//   C0 snapshot (taken as soon as this chunk's C update completes) at the end
+//   of the query phase.
 //
 //   CTA 1 ("GLA side") owns S (fp32 accumulator in tensor memory).  With
 //   Kh = K * exp(E) and Sb = Diag(exp R) S (R = the chunk's total log-decay):
@@ -102,7 +103,7 @@ __host__ __device__ constexpr uint32_t dot_off(int s, int row, int c) {
 }
 // UX: K-major B operand [80 rows][64 tokens]: row i < 64 holds ones at token
 // columns i' > i (the strictly-upper ones matrix, so LA^T U^T gives the
-// exclusive suffix sums), row 64 is all ones (chunk totals / column sums),
+// exclusive suffix sums), row 64 is all ones (the chunk totals R, CTA 1),
 // rows 65-79 are zero.
 
 struct Aux {
