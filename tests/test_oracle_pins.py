@@ -317,3 +317,77 @@ def test_rejects_bad_arguments():
         oracle.run("gla", **d, t0=5)          # t0 without a carried state
     with pytest.raises(ValueError):
         oracle.run("gdn", **{**d, "beta": None})
+
+
+# ----------------------------------------------------------------- backward oracle
+def _bwd_case(seed, B=1, H=2, T=9, dk=5, dv=4, state=True):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, H, T, dk))
+    k = rng.standard_normal((B, H, T, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((B, H, T, dv))
+    la = -np.abs(rng.standard_normal((B, H, T, dk))) / 8
+    w = rng.standard_normal((H, dk)) / np.sqrt(dk)
+    b = rng.standard_normal(H) * 0.1
+    S0 = rng.standard_normal((B, H, dk, dv)) * 0.3 if state else None
+    K0 = rng.standard_normal((B, H, 7, dk))
+    C0 = np.einsum("bhti,bhtj->bhij", K0, K0) if state else None
+    m0 = K0.sum(2) if state else None
+    return q, k, v, la, w, b, S0, C0, m0, (7 if state else 0)
+
+
+def test_backward_oracle_forward_equals_the_c_oracle():
+    """The autograd forward is an independent implementation of the same
+    recurrence: it must reproduce the C oracle's outputs and final state."""
+    import torch
+    from oracle.backward import forward_torch
+    q, k, v, la, w, b, S0, C0, m0, t0 = _bwd_case(1)
+    ref = oracle.run("gla", q, k, v, la, w, b, S0=S0, C0=C0, m0=m0, t0=t0)
+    for h in range(2):
+        T = lambda x: torch.as_tensor(x)  # noqa: E731
+        o, S, C, m = forward_torch(T(q[0, h]), T(k[0, h]), T(v[0, h]), T(la[0, h]), T(w[h]),
+                                   T(b[h]), None, T(S0[0, h]), T(C0[0, h]), T(m0[0, h]), t0)
+        np.testing.assert_allclose(o.numpy(), ref["o"][0, h], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(S.numpy(), ref["S"][0, h], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(C.numpy(), ref["C"][0, h], rtol=1e-12, atol=1e-12)
+
+
+def test_backward_oracle_matches_finite_differences():
+    import torch
+    from oracle.backward import forward_torch
+    q, k, v, la, w, b, S0, C0, m0, t0 = _bwd_case(2, T=3, dk=3, dv=2)
+    T = lambda x: torch.as_tensor(x[0, 0]).clone().requires_grad_()  # noqa: E731
+    args = [T(q), T(k), T(v), T(la), torch.as_tensor(w[0]).clone().requires_grad_(),
+            torch.as_tensor(b[0]).clone().requires_grad_()]
+    st = [T(S0), T(C0), T(m0)]
+
+    def f(*xs):
+        o, S, C, m = forward_torch(*xs[:6], None, *xs[6:], t0)
+        return o.sum() + (S * 0.3).sum() + (C * 0.1).sum() + m.sum()
+
+    assert torch.autograd.gradcheck(f, tuple(args + st), eps=1e-6, atol=1e-7, rtol=1e-5)
+
+
+def test_backward_oracle_plain_read_closed_forms():
+    """lambda = 0: o_t = S_t^T q_t, so dq_t = S_t do_t; one token from a zero
+    state: o = v (k . q), so dv = do (k . q) and dk = q (v . do)."""
+    from oracle.backward import gla_backward
+    q, k, v, la, w, b, S0, C0, m0, t0 = _bwd_case(3, state=False)
+    do = np.random.default_rng(4).standard_normal(v.shape)
+    lin = np.zeros(q.shape[:3])
+    g = gla_backward(q, k, v, la, w, b, do, lambda_in=lin)
+    fwd = oracle.run("gla", q, k, v, la, lambda_in=lin)
+    # S_t from the forward of each prefix
+    for t in range(q.shape[2]):
+        st = oracle.run("gla", q[:, :, :t + 1], k[:, :, :t + 1], v[:, :, :t + 1],
+                        la[:, :, :t + 1], lambda_in=lin[:, :, :t + 1])["S"]
+        np.testing.assert_allclose(g["dq"][:, :, t], np.einsum("bhij,bhj->bhi", st, do[:, :, t]),
+                                   rtol=1e-10, atol=1e-12)
+    assert fwd["o"].shape == do.shape
+    g1 = gla_backward(q[:, :, :1], k[:, :, :1], v[:, :, :1], la[:, :, :1], w, b, do[:, :, :1],
+                      lambda_in=lin[:, :, :1])
+    kq = (k[:, :, 0] * q[:, :, 0]).sum(-1)
+    np.testing.assert_allclose(g1["dv"][:, :, 0], do[:, :, 0] * kq[..., None], rtol=1e-12)
+    vd = (v[:, :, 0] * do[:, :, 0]).sum(-1)
+    np.testing.assert_allclose(g1["dk"][:, :, 0], q[:, :, 0] * vd[..., None], rtol=1e-12)
+    assert np.all(g1["dw_lambda"] == 0) and np.all(g1["db_lambda"] == 0)
