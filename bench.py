@@ -2,13 +2,15 @@
 fp32 state) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gla_fwd|gdn_fwd|gla_step|gdn_step|ccq_overhead|sigma_subspace]
+                    [--workload gla_fwd|gdn_fwd|gla_step|gdn_step|ccq_overhead|sigma_subspace|
+                                gla_bwd]
 
 Default (the headline): one step = one CCQ-GLA forward over the whole batch
 (read + gate + stats + GLA write/read, final state written).  The other
 workloads measure the rest of the library on their own JSON line: the Gated
 DeltaNet forward (B2 H16 T8192 d128) and the single-token decode steps
-(B64 H16 d128, state resident on the device and updated in place).
+(B64 H16 d128, state resident on the device and updated in place); gla_bwd
+times the gradients of the CCQ-GLA forward (fp32) on the headline's shape.
 ccq_overhead sweeps T = 2K..32K (B4 H16 d128) and reports the time of the
 CCQ-GLA forward over the plain GLA forward on the same pipeline.  Inputs are seeded synthetic data with
 the workload's distributions (anisotropic keys with one needle per sequence).
@@ -496,6 +498,153 @@ def run_subspace(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def bwd_flops_per_head_token(dk: int, dv: int) -> int:
+    """fp32 FLOPs of the two gradient sweeps per head-token (FMA = 2):
+    forward sweep 6 dk^2 + 5 dk dv (C update, C q, C gy; S update, S g),
+    reverse sweep 6 dk^2 + 7 dk dv (symmetric C adjoint update and product;
+    S adjoint update, its row and column products)."""
+    return 12 * dk * dk + 12 * dk * dv
+
+
+def oracle_bwd_sample(inp, go, w, max_seconds: float = 15.0):
+    """Time the fp64 gradient oracle (as it stands) on whole sequences of a
+    few (b, h) pairs, one after another on one host thread."""
+    from oracle.backward import gla_backward
+
+    n = lambda x: x.double().numpy()  # noqa: E731
+    pairs, dt = 0, 0.0
+    t0 = time.perf_counter()
+    for b in range(w.B):
+        for h in range(w.H):
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            gla_backward(n(inp["q"][sl]), n(inp["k"][sl]), n(inp["v"][sl]),
+                         n(inp["log_alpha"][sl]), n(inp["w_lambda"][h:h + 1]),
+                         n(inp["b_lambda"][h:h + 1]), n(go[sl]))
+            pairs += 1
+            dt = time.perf_counter() - t0
+            if dt > max_seconds:
+                break
+        if dt > max_seconds:
+            break
+    return {"value": pairs * w.T / w.H / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{pairs} of {w.B * w.H} (b,h) sequences x {w.T} tokens, fp64 autograd, "
+                      f"{dt:.1f} s; tokens/s = head-tokens/s / H"}, dt
+
+
+def run_bwd(args, world, rank, local):
+    """Gradients of the CCQ-GLA forward on B4 H16 T4096 dk = dv = 128, fp32:
+    one step = ccq_gla_bwd over the whole batch (forward sweep + reverse
+    sweep), all inputs and the upstream gradient resident in HBM."""
+    import ccq_read_side_gb300 as ccq
+    from ccq_read_side_gb300.workloads import WORKLOADS, Workload, make_inputs
+
+    w0 = WORKLOADS[WORKLOAD_INDEX]
+    w = Workload(w0.name.replace("bf16", "f32") + "_bwd", "gla", "f32", w0.B, w0.H, w0.T,
+                 w0.dk, w0.dv, w0.chunk, w0.seed, w0.keys)
+    inp = make_inputs(w)
+    go_cpu = torch.from_numpy(np.random.default_rng(w.seed + 1000)
+                              .standard_normal((w.B, w.H, w.T, w.dv)).astype(np.float32))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    go = go_cpu.to(dev)
+    stream = torch.cuda.current_stream()
+    ws = torch.empty(ccq.gla_bwd_workspace_bytes(w.B, w.H, w.T, w.dk, w.dv), dtype=torch.uint8,
+                     device=dev)
+
+    def step(dd=d, g=go):
+        return ccq.gla_bwd(dd["q"], dd["k"], dd["v"], dd["log_alpha"], dd["w_lambda"],
+                           dd["b_lambda"], g, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    total = max_over_ranks(sum(a.elapsed_time(b) * 1e-3 for a, b in ev), world)
+    t_step = total / args.steps
+    head_tokens = w.B * w.H * w.T
+    flops = bwd_flops_per_head_token(w.dk, w.dv) * head_tokens
+    fp32_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+
+    # e2e: inputs and upstream gradient copied from pinned host memory, the four
+    # token gradients copied back, every step
+    host = {k: inp[k].pin_memory() for k in ("q", "k", "v", "log_alpha", "w_lambda", "b_lambda")}
+    host["grad_o"] = go_cpu.pin_memory()
+    keys = list(host)
+    side = [torch.cuda.Stream(device=dev) for _ in keys]
+    dbuf = {k: torch.empty(host[k].shape, dtype=host[k].dtype, device=dev) for k in keys}
+    out_host = {k: torch.empty(host[k].shape, dtype=torch.float32).pin_memory()
+                for k in ("q", "k", "v", "log_alpha")}
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+
+    def e2e_step():
+        start = torch.cuda.Event()
+        start.record(stream)
+        for s_, k in zip(side, keys):
+            s_.wait_event(start)
+            with torch.cuda.stream(s_):
+                dbuf[k].copy_(host[k], non_blocking=True)
+            done = torch.cuda.Event()
+            done.record(s_)
+            stream.wait_event(done)
+        g = step(dbuf, dbuf["grad_o"])
+        for k, t in out_host.items():
+            t.copy_(g[k], non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(args.steps, 5))
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_t = max_over_ranks(e0.elapsed_time(e1) * 1e-3 / n_e2e, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu, _ = oracle_bwd_sample(inp, go_cpu, w)
+    if rank != 0:
+        return
+    tokens = w.B * w.T
+    line = {
+        "metric": "CCQ-GLA gradients tokens/s, H16 d128 T4K fp32, 1xGB300",
+        "value": tokens * world / t_step, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
+                   "l2": "inputs 671 MB > L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "alu", "achieved": flops / t_step / 1e12, "peak": fp32_peak,
+                     "unit": "TFLOP/s", "frac": flops / t_step / 1e12 / fp32_peak,
+                     "traffic": None,
+                     "flop_formula": "(12 dk^2 + 12 dk dv) fp32 FLOPs per head-token",
+                     "peak_source": "152 SMs x 128 fp32 lanes x 2 x 2.07 GHz (nominal)"},
+        "e2e": {"value": tokens * world / e2e_t, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+
+
 def ccq_launches_per_step() -> int:
     return 1  # one fused kernel launch per forward (or per decode step)
 
@@ -653,7 +802,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["gla_fwd", "gdn_fwd", "gla_step", "gdn_step",
-                                           "ccq_overhead", "sigma_subspace"],
+                                           "ccq_overhead", "sigma_subspace", "gla_bwd"],
                     default="gla_fwd")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -668,6 +817,8 @@ def main():
             run_overhead(args, world, rank, local)
         elif args.workload == "sigma_subspace":
             run_subspace(args, world, rank, local)
+        elif args.workload == "gla_bwd":
+            run_bwd(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

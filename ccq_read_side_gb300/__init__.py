@@ -16,8 +16,8 @@ from typing import Dict, Optional, Tuple
 
 import torch
 
-__all__ = ["gla_fwd", "gdn_fwd", "gla_step", "gdn_step", "sigma_subspace",
-           "subspace_alignment", "last_device_status", "status_string", "CcqError",
+__all__ = ["gla_fwd", "gdn_fwd", "gla_step", "gdn_step", "gla_bwd", "gla_bwd_workspace_bytes",
+           "sigma_subspace", "subspace_alignment", "last_device_status", "status_string", "CcqError",
            "library", "FLAG_L2NORM_QK", "FLAG_FP32_PATH", "FLAG_PLAIN_GLA", "FLAG_TEST_STALL",
            "STATUS"]
 
@@ -65,6 +65,11 @@ def library() -> ctypes.CDLL:
     lib.ccq_sigma_subspace.argtypes = [P, P, ctypes.c_int64, I, I, I, I, P, P, P]
     lib.ccq_subspace_alignment.restype = I
     lib.ccq_subspace_alignment.argtypes = [P, P, I, I, I, I, I, P, P]
+    lib.ccq_gla_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.ccq_gla_bwd_workspace_bytes.argtypes = [I, I, I, I, I]
+    lib.ccq_gla_bwd.restype = I
+    lib.ccq_gla_bwd.argtypes = ([P] * 10 + [ctypes.c_int64] + [P] * 14 + [ctypes.c_size_t]
+                                + [I] * 5 + [ctypes.c_uint, P])
     lib.ccq_status_string.restype = ctypes.c_char_p
     lib.ccq_status_string.argtypes = [I]
     lib.ccq_last_device_status.restype = I
@@ -271,3 +276,61 @@ def subspace_alignment(U, X, stream=None):
     if rc != 0:
         raise CcqError(rc, "ccq_subspace_alignment")
     return out
+
+
+def gla_bwd_workspace_bytes(B: int, H: int, T: int, dk: int, dv: int) -> int:
+    """Bytes of device workspace ccq_gla_bwd needs for these sizes."""
+    return int(library().ccq_gla_bwd_workspace_bytes(B, H, T, dk, dv))
+
+
+def gla_bwd(q, k, v, log_alpha, w_lambda, b_lambda, grad_o, *, lambda_in=None, S0=None, C0=None,
+            m0=None, t0: int = 0, grad_S=None, grad_C=None, grad_m=None,
+            want_state_grads: bool = False, workspace=None, stream=None) -> Dict:
+    """Gradients of the CCQ-GLA forward (fp32 tensors) for the loss
+    sum(o * grad_o) (+ final-state terms when grad_S / grad_C / grad_m are
+    given).  Returns a dict with q, k, v, log_alpha [B,H,T,*], w_lambda
+    [B,H,dk] and b_lambda [B,H] (one row per (b, h): sum over b for the
+    parameter gradient) and, if want_state_grads, S0, C0 (symmetric part),
+    m0.  `workspace`: a CUDA tensor of at least gla_bwd_workspace_bytes(...)
+    bytes (allocated here when None)."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dev = q.device
+    f32 = torch.float32
+    for name, t, shp in (("q", q, (B, H, T, dk)), ("k", k, (B, H, T, dk)),
+                         ("v", v, (B, H, T, dv)), ("log_alpha", log_alpha, (B, H, T, dk)),
+                         ("grad_o", grad_o, (B, H, T, dv))):
+        _need(t, name, f32, shp, dev)
+    _need(w_lambda, "w_lambda", f32, (H, dk), dev)
+    _need(b_lambda, "b_lambda", f32, (H,), dev)
+    _need(lambda_in, "lambda_in", f32, (B, H, T), dev)
+    _need(S0, "S0", f32, (B, H, dk, dv), dev)
+    _need(C0, "C0", f32, (B, H, dk, dk), dev)
+    _need(m0, "m0", f32, (B, H, dk), dev)
+    _need(grad_S, "grad_S", f32, (B, H, dk, dv), dev)
+    _need(grad_C, "grad_C", f32, (B, H, dk, dk), dev)
+    _need(grad_m, "grad_m", f32, (B, H, dk), dev)
+    need = gla_bwd_workspace_bytes(B, H, T, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", None, None, dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    g = {"q": torch.empty_like(q), "k": torch.empty_like(k), "v": torch.empty_like(v),
+         "log_alpha": torch.empty_like(log_alpha),
+         "w_lambda": torch.empty((B, H, dk), dtype=f32, device=dev),
+         "b_lambda": torch.empty((B, H), dtype=f32, device=dev)}
+    if want_state_grads:
+        g["S0"] = torch.empty((B, H, dk, dv), dtype=f32, device=dev)
+        g["C0"] = torch.empty((B, H, dk, dk), dtype=f32, device=dev)
+        g["m0"] = torch.empty((B, H, dk), dtype=f32, device=dev)
+    with torch.cuda.device(dev):
+        rc = library().ccq_gla_bwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(w_lambda), _ptr(b_lambda),
+            _ptr(lambda_in), _ptr(S0), _ptr(C0), _ptr(m0), int(t0), _ptr(grad_o), _ptr(grad_S),
+            _ptr(grad_C), _ptr(grad_m), _ptr(g["q"]), _ptr(g["k"]), _ptr(g["v"]),
+            _ptr(g["log_alpha"]), _ptr(g["w_lambda"]), _ptr(g["b_lambda"]), _ptr(g.get("S0")),
+            _ptr(g.get("C0")), _ptr(g.get("m0")), _ptr(workspace), ws_bytes, B, H, T, dk, dv, 0,
+            _stream(stream))
+    if rc != 0:
+        raise CcqError(rc, "ccq_gla_bwd")
+    return g

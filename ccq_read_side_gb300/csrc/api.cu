@@ -98,6 +98,10 @@ cudaError_t launch_sigma_subspace(const float *C, const float *m, double n, int 
 cudaError_t launch_alignment(const float *U, const void *X, bool bf16, int BH, int dk, int k,
                              int nx, float *align, cudaStream_t st);
 
+// Gradients of the CCQ-GLA forward (gla_bwd.cu).
+size_t gla_bwd_workspace_floats(long long BH, long long T, int dk);
+cudaError_t launch_gla_bwd(const BwdParams &p, int dk, int dv, cudaStream_t st);
+
 static ccq_status to_status(cudaError_t e) {
     if (e == cudaSuccess) return CCQ_OK;
     return CCQ_ERR_CUDA;
@@ -219,6 +223,48 @@ extern "C" ccq_status ccq_subspace_alignment(const float *U, const void *X, int 
     if (!U || !X || !align) return CCQ_ERR_INVALID_ARG;
     return to_status(launch_alignment(U, X, dtype == CCQ_DTYPE_BF16, BH, dk, k, nx, align,
                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+extern "C" size_t ccq_gla_bwd_workspace_bytes(int B, int H, int T, int dk, int dv) {
+    (void)dv;
+    if (B < 0 || H < 0 || T < 0 || dk < 1) return 0;
+    return sizeof(float) * gla_bwd_workspace_floats((long long)B * H, T, dk);
+}
+
+extern "C" ccq_status ccq_gla_bwd(
+    const float *q, const float *k, const float *v, const float *log_alpha,
+    const float *w_lambda, const float *b_lambda, const float *lambda_in, const float *S0,
+    const float *C0, const float *m0, int64_t t0, const float *grad_o, const float *grad_S,
+    const float *grad_C, const float *grad_m, float *grad_q, float *grad_k, float *grad_v,
+    float *grad_log_alpha, float *grad_w_lambda, float *grad_b_lambda, float *grad_S0,
+    float *grad_C0, float *grad_m0, void *workspace, size_t workspace_bytes, int B, int H, int T,
+    int dk, int dv, unsigned flags, ccq_stream_t stream) {
+    if (B < 0 || H < 0 || T < 0 || t0 < 0) return CCQ_ERR_INVALID_ARG;
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return CCQ_ERR_UNSUPPORTED;
+    if (flags != 0) return CCQ_ERR_INVALID_ARG;
+    if ((long long)B * H > 0x7fffffffLL || (long long)T + t0 > (1LL << 40))
+        return CCQ_ERR_UNSUPPORTED;
+    const int given = (S0 != nullptr) + (C0 != nullptr) + (m0 != nullptr);
+    if (given != 0 && given != 3) return CCQ_ERR_INVALID_ARG;
+    if (given == 0 && t0 != 0) return CCQ_ERR_INVALID_ARG;
+    const long long BH = (long long)B * H;
+    if (BH == 0) return CCQ_OK;
+    const bool tokens = T > 0;
+    if (tokens && (!q || !k || !v || !log_alpha || !grad_o || !grad_q || !grad_k || !grad_v ||
+                   !grad_log_alpha))
+        return CCQ_ERR_INVALID_ARG;
+    if (tokens && !lambda_in && (!w_lambda || !b_lambda)) return CCQ_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < sizeof(float) * gla_bwd_workspace_floats(BH, T, dk))
+        return CCQ_ERR_INVALID_ARG;
+    // token rows and the workspace are staged with 16-byte copies
+    auto al = [](const void *x) { return ((uintptr_t)x & 15u) == 0; };
+    if (!al(q) || !al(k) || !al(v) || !al(log_alpha) || !al(grad_o) || !al(workspace))
+        return CCQ_ERR_INVALID_ARG;
+    BwdParams p{q, k, v, log_alpha, w_lambda, b_lambda, lambda_in, S0, C0, m0, (long long)t0,
+                grad_o, grad_S, grad_C, grad_m, grad_q, grad_k, grad_v, grad_log_alpha,
+                grad_w_lambda, grad_b_lambda, grad_S0, grad_C0, grad_m0,
+                static_cast<float *>(workspace), (int)BH, H, T};
+    return to_status(launch_gla_bwd(p, dk, dv, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 extern "C" const char *ccq_status_string(ccq_status s) {

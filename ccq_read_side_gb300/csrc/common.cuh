@@ -53,3 +53,14 @@ struct CcqParams {
     unsigned flags;
     unsigned int *status;  // device status word of the current device
 };
+
+// Parameters of the gradient kernels (gla_bwd.cu).
+struct BwdParams {
+    const float *q, *k, *v, *log_alpha, *w_lambda, *b_lambda, *lambda_in;
+    const float *S0, *C0, *m0;
+    long long t0;
+    const float *grad_o, *grad_S, *grad_C, *grad_m;
+    float *grad_q, *grad_k, *grad_v, *grad_la, *grad_w, *grad_b, *grad_S0, *grad_C0, *grad_m0;
+    float *ws;  // workspace: qc, gy, qc*gqc [BH][T][dk]; scalars [BH][T][4]; rs [BH][dk]
+    int BH, H, T;
+};

@@ -60,6 +60,7 @@
 #ifndef CCQ_H_
 #define CCQ_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -177,6 +178,41 @@ ccq_status ccq_sigma_subspace(const float *C, const float *m, int64_t n, int BH,
  */
 ccq_status ccq_subspace_alignment(const float *U, const void *X, int BH, int dk, int k, int nx,
                                   ccq_dtype dtype, float *align, ccq_stream_t stream);
+
+/*
+ * Gradients of the CCQ-GLA forward (the operator of ccq_gla_fwd, float32
+ * arithmetic on CUDA cores, float32 tensors only).  For the loss
+ *   L = sum(o * grad_o) + sum(S_T * grad_S) + sum(C_T * grad_C) + sum(m_T * grad_m)
+ * it writes
+ *   grad_q, grad_k, grad_log_alpha [B,H,T,dk];  grad_v [B,H,T,dv]   (required)
+ *   grad_w_lambda [B,H,dk], grad_b_lambda [B,H]: one row per (b, h), to be
+ *     summed over b by the caller (nullable; zero when lambda_in is given)
+ *   grad_S0 [B,H,dk,dv], grad_m0 [B,H,dk] (nullable)
+ *   grad_C0 [B,H,dk,dk] (nullable): the gradient with respect to a symmetric
+ *     C0, i.e. the symmetric part of the unconstrained one (C is a sum of
+ *     k k^T; only the symmetric part of grad_C matters, and C0 must be
+ *     symmetric).
+ * Inputs as ccq_gla_fwd (float32; q, k, v, log_alpha, grad_o 16-byte
+ * aligned); grad_S, grad_C, grad_m nullable (zero).  The gradients are those
+ * of the forward's definition (the read after the write; Sigma_t with n_t =
+ * t0 + t + 1); the method's pages describe the forward only, the backward is
+ * its derivative.
+ * workspace: device memory of at least ccq_gla_bwd_workspace_bytes(B, H, T,
+ * dk, dv) bytes (3 dk + 4 floats per token and head, plus dk per head),
+ * 16-byte aligned, owned by the caller, overwritten.  Two kernels run in
+ * stream order (a forward sweep that fills the workspace, then a reverse
+ * sweep).  flags must be 0.  dk, dv in {64, 128}.  Returns as ccq_gla_fwd.
+ */
+size_t ccq_gla_bwd_workspace_bytes(int B, int H, int T, int dk, int dv);
+ccq_status ccq_gla_bwd(const float *q, const float *k, const float *v, const float *log_alpha,
+                       const float *w_lambda, const float *b_lambda, const float *lambda_in,
+                       const float *S0, const float *C0, const float *m0, int64_t t0,
+                       const float *grad_o, const float *grad_S, const float *grad_C,
+                       const float *grad_m, float *grad_q, float *grad_k, float *grad_v,
+                       float *grad_log_alpha, float *grad_w_lambda, float *grad_b_lambda,
+                       float *grad_S0, float *grad_C0, float *grad_m0, void *workspace,
+                       size_t workspace_bytes, int B, int H, int T, int dk, int dv,
+                       unsigned flags, ccq_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char *ccq_status_string(ccq_status s);

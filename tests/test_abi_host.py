@@ -160,3 +160,36 @@ def test_subspace_diagnostics_validate_synchronously(lib):
     assert lib.ccq_subspace_alignment(FAKE, FAKE, 1, 128, 16, 4, 7, FAKE, None) == 2
     assert lib.ccq_subspace_alignment(None, FAKE, 1, 128, 16, 4, 1, FAKE, None) == 1
     assert lib.ccq_subspace_alignment(None, None, 0, 128, 16, 4, 1, None, None) == 0
+
+
+def _bwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, la=FAKE, w=FAKE, b=FAKE, lin=None, S0=None, C0=None,
+             m0=None, t0=0, go=FAKE, gS=None, gC=None, gm=None, gq=FAKE, gk=FAKE, gv=FAKE,
+             gla=FAKE, gw=None, gb=None, gS0=None, gC0=None, gm0=None, ws=FAKE, ws_bytes=1 << 40,
+             B=1, H=1, T=8, dk=64, dv=64, flags=0, stream=None)
+    a.update(kw)
+    return lib.ccq_gla_bwd(*a.values())
+
+
+def test_backward_workspace_size(lib):
+    # 3 dk + 4 floats per token and head, dk per head
+    assert lib.ccq_gla_bwd_workspace_bytes(2, 3, 10, 64, 128) == 4 * (6 * 10 * (3 * 64 + 4) + 6 * 64)
+    assert lib.ccq_gla_bwd_workspace_bytes(1, 1, 0, 128, 128) == 4 * 128
+    assert lib.ccq_gla_bwd_workspace_bytes(-1, 1, 0, 128, 128) == 0
+
+
+@pytest.mark.parametrize("case,code", [
+    (dict(dk=96), 2),
+    (dict(flags=1), 1),
+    (dict(ws=None), 1),
+    (dict(ws_bytes=16), 1),
+    (dict(q=ctypes.c_void_p(0x1004)), 1),          # token rows are staged 16 bytes at a time
+    (dict(S0=FAKE), 1),                            # S0, C0, m0 all or none
+    (dict(t0=5), 1),                               # a token count without a state
+    (dict(w=None), 1),                             # the gate needs w and b ...
+    (dict(w=None, b=None, lin=FAKE, ws=None), 1),  # ... unless lambda is given
+    (dict(gq=None), 1),
+    (dict(B=0, q=None, k=None, v=None, la=None, go=None, ws=None), 0),  # empty batch: no CUDA call
+])
+def test_backward_validates_synchronously(lib, case, code):
+    assert _bwd(lib, **case) == code
