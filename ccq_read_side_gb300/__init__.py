@@ -29,7 +29,7 @@ FLAG_FP32_PATH = 2
 FLAG_PLAIN_GLA = 4  # measurement baseline: plain GLA read, no key statistics
 FLAG_TEST_STALL = 0x100  # test only: makes the tensor-core kernel's bounded waits run out
 STATUS = {0: "CCQ_OK", 1: "CCQ_ERR_INVALID_ARG", 2: "CCQ_ERR_UNSUPPORTED", 3: "CCQ_ERR_CUDA",
-          4: "CCQ_ERR_TIMEOUT", 5: "CCQ_ERR_RANGE"}
+          4: "CCQ_ERR_TIMEOUT", 5: "CCQ_ERR_RANGE", 6: "CCQ_ERR_TOO_LARGE"}
 _DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 
 _lib = None
@@ -70,6 +70,9 @@ def library() -> ctypes.CDLL:
     lib.ccq_gla_bwd.restype = I
     lib.ccq_gla_bwd.argtypes = ([P] * 10 + [ctypes.c_int64] + [P] * 14 + [ctypes.c_size_t]
                                 + [I] * 5 + [ctypes.c_uint, P])
+    lib.ccq_gla_bwd_noalloc.restype = I
+    lib.ccq_gla_bwd_noalloc.argtypes = ([P] * 10 + [ctypes.c_int64] + [P] * 13 + [I] * 5
+                                        + [ctypes.c_uint, P])
     lib.ccq_status_string.restype = ctypes.c_char_p
     lib.ccq_status_string.argtypes = [I]
     lib.ccq_last_device_status.restype = I

@@ -275,6 +275,8 @@ extern "C" const char *ccq_status_string(ccq_status s) {
         case CCQ_ERR_CUDA: return "CCQ_ERR_CUDA: a CUDA call failed";
         case CCQ_ERR_TIMEOUT: return "CCQ_ERR_TIMEOUT: a bounded wait in a kernel gave up";
         case CCQ_ERR_RANGE: return "CCQ_ERR_RANGE: chunk log-decay outside the tensor-core range";
+        case CCQ_ERR_TOO_LARGE:
+            return "CCQ_ERR_TOO_LARGE: sizes exceed the fixed scratch of a no-allocation entry point";
     }
     return "CCQ: unknown status";
 }

@@ -37,6 +37,8 @@
 // Shapes: dk, dv in {64, 128}; any T (a ragged last chunk); 256 threads.
 // Token vectors are staged TL tokens at a time with cp.async (16-byte
 // copies, double-buffered) so each chunk's loads overlap the previous chunk.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace ccq {
@@ -441,3 +443,55 @@ cudaError_t launch_gla_bwd(const BwdParams &p, int dk, int dv, cudaStream_t st) 
 }
 
 }  // namespace ccq
+
+// ---- ccq_gla_bwd_noalloc: the same two kernels on a fixed scratch array --
+//
+// For callers that must not allocate device memory on the call path (a
+// runtime that hands all device memory to its own allocator up front, or
+// latency-bound code that cannot take the implicit device synchronisation of
+// cudaMalloc and cudaFree): the workspace is this file-scope array, sized by
+// CCQ_GLA_BWD_NOALLOC_SCRATCH_BYTES.  Nothing in it needs to start at zero:
+// the forward sweep writes every word the reverse sweep reads.  Every call on
+// a device shares it, so calls whose kernels overlap on the GPU race.
+static __device__ __align__(256) float ccq_bwd_scratch[CCQ_GLA_BWD_NOALLOC_SCRATCH_BYTES /
+                                                        sizeof(float)];
+
+namespace {
+std::mutex scratch_mu;
+void *scratch_ptr[64] = {};
+
+// Device address of ccq_bwd_scratch on the current device, looked up on the
+// first call on that device and kept.
+void *static_scratch() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(scratch_mu);
+    if (!scratch_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress((void **)&ptr, ccq_bwd_scratch) != cudaSuccess) return nullptr;
+        scratch_ptr[dev] = ptr;
+    }
+    return scratch_ptr[dev];
+}
+}  // namespace
+
+extern "C" ccq_status ccq_gla_bwd_noalloc(
+    const float *q, const float *k, const float *v, const float *log_alpha,
+    const float *w_lambda, const float *b_lambda, const float *lambda_in, const float *S0,
+    const float *C0, const float *m0, int64_t t0, const float *grad_o, const float *grad_S,
+    const float *grad_C, const float *grad_m, float *grad_q, float *grad_k, float *grad_v,
+    float *grad_log_alpha, float *grad_w_lambda, float *grad_b_lambda, float *grad_S0,
+    float *grad_C0, float *grad_m0, int B, int H, int T, int dk, int dv, unsigned flags,
+    ccq_stream_t stream) {
+    const size_t need = ccq_gla_bwd_workspace_bytes(B, H, T, dk, dv);
+    if (need > (size_t)CCQ_GLA_BWD_NOALLOC_SCRATCH_BYTES) return CCQ_ERR_TOO_LARGE;
+    void *ws = nullptr;
+    if (B > 0 && H > 0) {  // no CUDA call for an empty batch or a rejected size
+        ws = static_scratch();
+        if (!ws) return CCQ_ERR_CUDA;
+    }
+    return ccq_gla_bwd(q, k, v, log_alpha, w_lambda, b_lambda, lambda_in, S0, C0, m0, t0, grad_o,
+                       grad_S, grad_C, grad_m, grad_q, grad_k, grad_v, grad_log_alpha,
+                       grad_w_lambda, grad_b_lambda, grad_S0, grad_C0, grad_m0, ws,
+                       (size_t)CCQ_GLA_BWD_NOALLOC_SCRATCH_BYTES, B, H, T, dk, dv, flags, stream);
+}

@@ -75,8 +75,10 @@ typedef enum {
     CCQ_ERR_UNSUPPORTED = 2, /* shape or dtype outside the supported set */
     CCQ_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed (launch, attribute, map) */
     CCQ_ERR_TIMEOUT = 4,     /* device: a bounded wait inside a kernel gave up */
-    CCQ_ERR_RANGE = 5        /* device: a chunk's cumulative log-decay exceeded the
+    CCQ_ERR_RANGE = 5,       /* device: a chunk's cumulative log-decay exceeded the
                                 tensor-core path's exponent range (|sum| > 80) */
+    CCQ_ERR_TOO_LARGE = 6    /* sizes need more scratch than a no-allocation entry
+                                point's fixed array holds */
 } ccq_status;
 
 typedef enum { CCQ_DTYPE_F32 = 0, CCQ_DTYPE_BF16 = 1 } ccq_dtype;
@@ -213,6 +215,39 @@ ccq_status ccq_gla_bwd(const float *q, const float *k, const float *v, const flo
                        float *grad_S0, float *grad_C0, float *grad_m0, void *workspace,
                        size_t workspace_bytes, int B, int H, int T, int dk, int dv,
                        unsigned flags, ccq_stream_t stream);
+
+/*
+ * ccq_gla_bwd without a workspace argument, for callers that must not
+ * allocate device memory on the call path: a runtime that gives all device
+ * memory to its own allocator at start-up, or latency-bound code that cannot
+ * take the implicit device synchronisation of cudaMalloc / cudaFree.  The
+ * method's pages have no counterpart to this entry point; it is a property of
+ * the library, not of the operator.
+ * The workspace is a fixed array inside the library, one per device, of
+ * CCQ_GLA_BWD_NOALLOC_SCRATCH_BYTES bytes: sizes whose
+ * ccq_gla_bwd_workspace_bytes exceeds it return CCQ_ERR_TOO_LARGE without any
+ * CUDA call (at dk = 128 that is about 10,800 token-heads, e.g. B1 H2 T4096;
+ * at dk = 64 about 21,000).  The call allocates nothing (no cudaMalloc, no
+ * cudaFree, no allocating library routine).
+ * The first call on a device (with that device current, B*H > 0) looks up
+ * the array's device address with cudaGetSymbolAddress and keeps it; make
+ * that first call before any stream capture.  Every call on a device shares
+ * the one array: calls whose kernels overlap on the GPU (other streams, other
+ * host threads) race and give wrong results, so serialise them (one stream,
+ * or an event between calls).  Nothing in the array needs to start at zero.
+ * Arguments, results and the other errors as ccq_gla_bwd.
+ */
+#define CCQ_GLA_BWD_NOALLOC_SCRATCH_BYTES (16u << 20)
+ccq_status ccq_gla_bwd_noalloc(const float *q, const float *k, const float *v,
+                               const float *log_alpha, const float *w_lambda,
+                               const float *b_lambda, const float *lambda_in, const float *S0,
+                               const float *C0, const float *m0, int64_t t0,
+                               const float *grad_o, const float *grad_S, const float *grad_C,
+                               const float *grad_m, float *grad_q, float *grad_k, float *grad_v,
+                               float *grad_log_alpha, float *grad_w_lambda,
+                               float *grad_b_lambda, float *grad_S0, float *grad_C0,
+                               float *grad_m0, int B, int H, int T, int dk, int dv,
+                               unsigned flags, ccq_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char *ccq_status_string(ccq_status s);
