@@ -58,12 +58,12 @@ namespace ccq {
 
 namespace bwd {
 
-// CTA size and chunk length of the two sweeps: 512 threads (16 warps, so
-// each SM has warps to switch to while one waits on shared memory); the
-// forward sweep takes 16-token chunks (one warp per token), the reverse
-// sweep 8-token chunks (its chunk buffers and partial products are larger).
-constexpr int NT_F = 512, TL_F = 16;
-constexpr int NT_R = 512, TL_R = 8;
+// CTA size and chunk length of the two sweeps: 8 warps, one per token of an
+// 8-token chunk.  Each thread owns a tile of several rows by a slice of
+// columns of the state, so that one vector loaded from shared memory feeds
+// every row of the tile.
+constexpr int NT_F = 256, TL_F = 8;
+constexpr int NT_R = 256, TL_R = 8;
 
 __device__ __forceinline__ void cp16(float *dst, const float *src) {
     const unsigned s = (unsigned)__cvta_generic_to_shared(dst);
@@ -94,37 +94,43 @@ struct Ws {
     }
 };
 
-template <int DK, int DV, int NT = NT_F, int TL = TL_F>
-__global__ void __launch_bounds__(NT, 1) fwd_sweep_kernel(const BwdParams p) {
-    constexpr int NP = NT / DK, RC = DK / NP, RS = DV / NP, XL = DK / 32;
-    constexpr int BUF = TL * (3 * DK + 2 * DV) + TL;  // q k la | v g | lambda
-    static_assert(NT / 32 == TL, "one warp per token of a chunk");
+template <int DK, int DV>
+__global__ void __launch_bounds__(NT_F, 1) fwd_sweep_kernel(const BwdParams p) {
+    constexpr int NT = NT_F, TL = TL_F, NP = NT / 32;  // 8 warps = 8 column slices
+    constexpr int RX = DK / 32, CW = DK / NP, SW = DV / NP, XL = DK / 32;
+    constexpr int RED = NP * DK;                       // partial products per token
+    constexpr int BUF = TL * (3 * DK + 2 * DV) + TL;   // q k la | v g | lambda
+    static_assert(NP == TL && CW % 4 == 0 && SW % 4 == 0, "one warp per token of a chunk");
     extern __shared__ float4 smem_f4[];
     float *sm = reinterpret_cast<float *>(smem_f4);
-    float *red1 = sm + 2 * BUF;     // [TL][NT]  C_u q_u partials, by (x, part)
-    float *red2 = red1 + TL * NT;   // [TL][NT]  S_u g_u partials
-    float *red3 = red2 + TL * NT;   // [TL][NT]  C_end gy_u partials
-    float *mb = red3 + TL * NT;     // [TL][DK]  m after token u
-    float *gyb = mb + TL * DK;      // [TL][DK]  gy_u
-    float *dmat = gyb + TL * DK;    // [TL][TL]  k_u' . gy_u (u' > u)
-    const int tid = threadIdx.x, x = tid % DK, part = tid / DK, lane = tid & 31, warp = tid >> 5;
+    float *red1 = sm + 2 * BUF;     // [TL][NP][DK]  C_u q_u partials
+    float *red2 = red1 + TL * RED;  // [TL][NP][DK]  S_u g_u partials
+    float *red3 = red2 + TL * RED;  // [TL][NP][DK]  C_end gy_u partials
+    float *mb = red3 + TL * RED;    // [TL][DK]      m after token u
+    float *gyb = mb + TL * DK;      // [TL][DK]      gy_u
+    float *dmat = gyb + TL * DK;    // [TL][TL]      k_u' . gy_u (u' > u)
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, part = warp;
     const int bh = blockIdx.x, h = bh % p.H, T = p.T;
     const size_t tok0 = (size_t)bh * T;
     const Ws ws(p, DK);
     const bool gate = p.lambda_in == nullptr;
 
-    float Cr[RC], Sr[RS];  // C[x][part*RC + r],  S[x][part*RS + r]
+    // thread tile: rows x_i = lane + 32 i of C (columns part*CW ..) and of S
+    // (columns part*SW ..)
+    float Cr[RX][CW], Sr[RX][SW];
 #pragma unroll
-    for (int r = 0; r < RC; ++r)
-        Cr[r] = p.C0 ? p.C0[((size_t)bh * DK + x) * DK + part * RC + r] : 0.f;
+    for (int i = 0; i < RX; ++i) {
+        const size_t row = (size_t)bh * DK + lane + 32 * i;
 #pragma unroll
-    for (int r = 0; r < RS; ++r)
-        Sr[r] = p.S0 ? p.S0[((size_t)bh * DK + x) * DV + part * RS + r] : 0.f;
-    float m_x = (part == 0 && p.m0) ? p.m0[(size_t)bh * DK + x] : 0.f;
-    // per-lane values of the warp-per-token phases: channel x = lane + 32 i
-    float wl[XL], dw[XL];
+        for (int r = 0; r < CW; ++r) Cr[i][r] = p.C0 ? p.C0[row * DK + part * CW + r] : 0.f;
+#pragma unroll
+        for (int r = 0; r < SW; ++r) Sr[i][r] = p.S0 ? p.S0[row * DV + part * SW + r] : 0.f;
+    }
+    // the same lanes carry channel x = lane + 32 i in the warp-per-token phases
+    float m_r[RX], wl[XL], dw[XL];
 #pragma unroll
     for (int i = 0; i < XL; ++i) {
+        m_r[i] = (part == 0 && p.m0) ? p.m0[(size_t)bh * DK + lane + 32 * i] : 0.f;
         wl[i] = gate ? p.w_lambda[h * DK + lane + 32 * i] : 0.f;
         dw[i] = 0.f;
     }
@@ -155,43 +161,60 @@ __global__ void __launch_bounds__(NT, 1) fwd_sweep_kernel(const BwdParams p) {
         const float *V = b + 3 * TL * DK, *G = V + TL * DV, *LAM = G + TL * DV;
         const int tc = c * TL, n = min(TL, T - tc);
 
-        // (A) the write, token by token, in registers: C += k k^T and
-        //     S = Diag(alpha) S + k v^T on the owned rows, with the partial
-        //     products C_u q_u and S_u g_u of every token
+        // (A) the write, token by token, on the thread's tiles: C += k k^T,
+        //     S = Diag(alpha) S + k v^T, with the partial products C_u q_u and
+        //     S_u g_u of every token (one loaded k, q, v, g vector serves RX rows)
         for (int u = 0; u < n; ++u) {
             const float *qv = Q + u * DK, *kv = K + u * DK, *vv = V + u * DV, *gv = G + u * DV;
-            const float kx = kv[x], ax = expf(LA[u * DK + x]);
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            float kx[RX], ax[RX], a[RX], s[RX];
 #pragma unroll
-            for (int r = 0; r < RC; r += 4) {
-                const float4 k4 = ld4(kv + part * RC + r), q4 = ld4(qv + part * RC + r);
-                Cr[r] = fmaf(k4.x, kx, Cr[r]);
-                Cr[r + 1] = fmaf(k4.y, kx, Cr[r + 1]);
-                Cr[r + 2] = fmaf(k4.z, kx, Cr[r + 2]);
-                Cr[r + 3] = fmaf(k4.w, kx, Cr[r + 3]);
-                a0 = fmaf(Cr[r], q4.x, a0);
-                a1 = fmaf(Cr[r + 1], q4.y, a1);
-                a2 = fmaf(Cr[r + 2], q4.z, a2);
-                a3 = fmaf(Cr[r + 3], q4.w, a3);
+            for (int i = 0; i < RX; ++i) {
+                kx[i] = kv[lane + 32 * i];
+                ax[i] = expf(LA[u * DK + lane + 32 * i]);
+                a[i] = 0.f;
+                s[i] = 0.f;
             }
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-            for (int r = 0; r < RS; r += 4) {
-                const float4 v4 = ld4(vv + part * RS + r), g4 = ld4(gv + part * RS + r);
-                Sr[r] = fmaf(ax, Sr[r], kx * v4.x);
-                Sr[r + 1] = fmaf(ax, Sr[r + 1], kx * v4.y);
-                Sr[r + 2] = fmaf(ax, Sr[r + 2], kx * v4.z);
-                Sr[r + 3] = fmaf(ax, Sr[r + 3], kx * v4.w);
-                s0 = fmaf(Sr[r], g4.x, s0);
-                s1 = fmaf(Sr[r + 1], g4.y, s1);
-                s2 = fmaf(Sr[r + 2], g4.z, s2);
-                s3 = fmaf(Sr[r + 3], g4.w, s3);
+            for (int r = 0; r < CW; r += 4) {
+                const float4 k4 = ld4(kv + part * CW + r), q4 = ld4(qv + part * CW + r);
+#pragma unroll
+                for (int i = 0; i < RX; ++i) {
+                    Cr[i][r] = fmaf(k4.x, kx[i], Cr[i][r]);
+                    Cr[i][r + 1] = fmaf(k4.y, kx[i], Cr[i][r + 1]);
+                    Cr[i][r + 2] = fmaf(k4.z, kx[i], Cr[i][r + 2]);
+                    Cr[i][r + 3] = fmaf(k4.w, kx[i], Cr[i][r + 3]);
+                    a[i] = fmaf(Cr[i][r], q4.x, a[i]);
+                    a[i] = fmaf(Cr[i][r + 1], q4.y, a[i]);
+                    a[i] = fmaf(Cr[i][r + 2], q4.z, a[i]);
+                    a[i] = fmaf(Cr[i][r + 3], q4.w, a[i]);
+                }
             }
-            red1[u * NT + part * DK + x] = (a0 + a1) + (a2 + a3);
-            red2[u * NT + part * DK + x] = (s0 + s1) + (s2 + s3);
+#pragma unroll
+            for (int r = 0; r < SW; r += 4) {
+                const float4 v4 = ld4(vv + part * SW + r), g4 = ld4(gv + part * SW + r);
+#pragma unroll
+                for (int i = 0; i < RX; ++i) {
+                    Sr[i][r] = fmaf(ax[i], Sr[i][r], kx[i] * v4.x);
+                    Sr[i][r + 1] = fmaf(ax[i], Sr[i][r + 1], kx[i] * v4.y);
+                    Sr[i][r + 2] = fmaf(ax[i], Sr[i][r + 2], kx[i] * v4.z);
+                    Sr[i][r + 3] = fmaf(ax[i], Sr[i][r + 3], kx[i] * v4.w);
+                    s[i] = fmaf(Sr[i][r], g4.x, s[i]);
+                    s[i] = fmaf(Sr[i][r + 1], g4.y, s[i]);
+                    s[i] = fmaf(Sr[i][r + 2], g4.z, s[i]);
+                    s[i] = fmaf(Sr[i][r + 3], g4.w, s[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RX; ++i) {
+                red1[u * RED + part * DK + lane + 32 * i] = a[i];
+                red2[u * RED + part * DK + lane + 32 * i] = s[i];
+            }
             if (part == 0) {
-                m_x += kx;
-                mb[u * DK + x] = m_x;
+#pragma unroll
+                for (int i = 0; i < RX; ++i) {
+                    m_r[i] += kx[i];
+                    mb[u * DK + lane + 32 * i] = m_r[i];
+                }
             }
         }
         __syncthreads();
@@ -211,8 +234,8 @@ __global__ void __launch_bounds__(NT, 1) fwd_sweep_kernel(const BwdParams p) {
                 gqc[i] = 0.f;
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
-                    cq[i] += red1[u * NT + j * DK + xi];
-                    gqc[i] += red2[u * NT + j * DK + xi];
+                    cq[i] += red1[u * RED + j * DK + xi];
+                    gqc[i] += red2[u * RED + j * DK + xi];
                 }
                 mq = fmaf(mb[u * DK + xi], qv[xi], mq);
                 z = fmaf(wl[i], qv[xi], z);
@@ -236,29 +259,43 @@ __global__ void __launch_bounds__(NT, 1) fwd_sweep_kernel(const BwdParams p) {
             }
             gl = warp_sum(glp);
             mg = warp_sum(mgp);
-            // k_u' . gy_u for the later tokens of the chunk: C_u = C_end - sum_{u'>u} k k^T
-            for (int up = u + 1; up < n; ++up) {
-                float s = 0.f;
-#pragma unroll
-                for (int i = 0; i < XL; ++i) s = fmaf(K[up * DK + lane + 32 * i], gy[i], s);
-                s = warp_sum(s);
-                if (lane == 0) dmat[up * TL + u] = s;
-            }
         }
         __syncthreads();
 
-        // (C) C_end gy_u for every token, on the owned rows
+        // (C) C_end gy_u for every token, on the thread's tile of C
         for (int v_ = 0; v_ < n; ++v_) {
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            float a[RX];
 #pragma unroll
-            for (int r = 0; r < RC; r += 4) {
-                const float4 y4 = ld4(gyb + v_ * DK + part * RC + r);
-                a0 = fmaf(Cr[r], y4.x, a0);
-                a1 = fmaf(Cr[r + 1], y4.y, a1);
-                a2 = fmaf(Cr[r + 2], y4.z, a2);
-                a3 = fmaf(Cr[r + 3], y4.w, a3);
+            for (int i = 0; i < RX; ++i) a[i] = 0.f;
+#pragma unroll
+            for (int r = 0; r < CW; r += 4) {
+                const float4 y4 = ld4(gyb + v_ * DK + part * CW + r);
+#pragma unroll
+                for (int i = 0; i < RX; ++i) {
+                    a[i] = fmaf(Cr[i][r], y4.x, a[i]);
+                    a[i] = fmaf(Cr[i][r + 1], y4.y, a[i]);
+                    a[i] = fmaf(Cr[i][r + 2], y4.z, a[i]);
+                    a[i] = fmaf(Cr[i][r + 3], y4.w, a[i]);
+                }
             }
-            red3[v_ * NT + part * DK + x] = (a0 + a1) + (a2 + a3);
+#pragma unroll
+            for (int i = 0; i < RX; ++i) red3[v_ * RED + part * DK + lane + 32 * i] = a[i];
+        }
+        // k_u' . gy_u for u < u' (C_u = C_end - sum_{u'>u} k_u' k_u'^T), the
+        // TL (TL - 1) / 2 pairs dealt round-robin over the warps
+        for (int pr = warp; pr < TL * (TL - 1) / 2; pr += NT / 32) {
+            int up = 1, uu = pr;
+            while (uu >= up) {
+                uu -= up;
+                ++up;
+            }
+            if (up >= n) continue;  // warp-uniform
+            float s_ = 0.f;
+#pragma unroll
+            for (int i = 0; i < XL; ++i)
+                s_ = fmaf(K[up * DK + lane + 32 * i], gyb[uu * DK + lane + 32 * i], s_);
+            s_ = warp_sum(s_);
+            if (lane == 0) dmat[up * TL + uu] = s_;
         }
         __syncthreads();
 
@@ -271,7 +308,7 @@ __global__ void __launch_bounds__(NT, 1) fwd_sweep_kernel(const BwdParams p) {
                 const int xi = lane + 32 * i;
                 float cgy = 0.f;
 #pragma unroll
-                for (int j = 0; j < NP; ++j) cgy += red3[u * NT + j * DK + xi];
+                for (int j = 0; j < NP; ++j) cgy += red3[u * RED + j * DK + xi];
                 for (int up = u + 1; up < n; ++up) cgy -= K[up * DK + xi] * dmat[up * TL + u];
                 const size_t o = (tok0 + t) * DK + xi;
                 p.grad_q[o] = gqc[i] + (cgy * rn - mu[i] * mg) + gz * wl[i];
@@ -289,27 +326,35 @@ __global__ void __launch_bounds__(NT, 1) fwd_sweep_kernel(const BwdParams p) {
     }
     // rowsum(dL/dS_T * S_T): the final state's share of the decay gradient;
     // the gate gradients summed over the warps
-    float rs = 0.f;
-    if (p.grad_S) {
+    float rs[RX];
 #pragma unroll
-        for (int r = 0; r < RS; ++r)
-            rs = fmaf(p.grad_S[((size_t)bh * DK + x) * DV + part * RS + r], Sr[r], rs);
+    for (int i = 0; i < RX; ++i) {
+        rs[i] = 0.f;
+        if (p.grad_S) {
+            const size_t row = (size_t)bh * DK + lane + 32 * i;
+#pragma unroll
+            for (int r = 0; r < SW; ++r)
+                rs[i] = fmaf(p.grad_S[row * DV + part * SW + r], Sr[i][r], rs[i]);
+        }
     }
     __syncthreads();
-    red1[part * DK + x] = rs;
 #pragma unroll
-    for (int i = 0; i < XL; ++i) red2[warp * DK + lane + 32 * i] = dw[i];
+    for (int i = 0; i < RX; ++i) {
+        red1[part * DK + lane + 32 * i] = rs[i];
+        red2[warp * DK + lane + 32 * i] = dw[i];
+    }
     if (lane == 0) red2[TL * DK + warp] = db;
     __syncthreads();
     if (tid < DK) {
         float s = 0.f, w_ = 0.f;
 #pragma unroll
-        for (int j = 0; j < NP; ++j) s += red1[j * DK + x];
-#pragma unroll
-        for (int j = 0; j < TL; ++j) w_ += red2[j * DK + x];
-        ws.rs[(size_t)bh * DK + x] = s;
-        if (p.grad_w) p.grad_w[(size_t)bh * DK + x] = w_;
-        if (p.grad_b && x == 0) {
+        for (int j = 0; j < NP; ++j) {
+            s += red1[j * DK + tid];
+            w_ += red2[j * DK + tid];
+        }
+        ws.rs[(size_t)bh * DK + tid] = s;
+        if (p.grad_w) p.grad_w[(size_t)bh * DK + tid] = w_;
+        if (p.grad_b && tid == 0) {
             float b_ = 0.f;
             for (int j = 0; j < TL; ++j) b_ += red2[TL * DK + j];
             p.grad_b[bh] = b_;
@@ -317,47 +362,56 @@ __global__ void __launch_bounds__(NT, 1) fwd_sweep_kernel(const BwdParams p) {
     }
 }
 
-template <int DK, int DV, int NT = NT_R, int TL = TL_R>
-__global__ void __launch_bounds__(NT, 1) rev_sweep_kernel(const BwdParams p) {
-    constexpr int NP = NT / DK, RC = DK / NP, RS = DV / NP, XL = DK / 32, YL = DV / 32;
-    constexpr int NPV = NT / DV, RV = DK / NPV;
+template <int DK, int DV>
+__global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
+    constexpr int NT = NT_R, TL = TL_R, NP = 4;   // 8 warps: 4 column slices x 2 row halves
+    constexpr int RX = DK / 64, CW = DK / NP, SW = DV / NP;   // row tiles of G and GS
+    constexpr int YX = DV / 64, RW = DK / NP;                // column tiles of the entry state
+    constexpr int XL = DK / 32, YL = DV / 32;
+    constexpr int RED = NP * DK, REDV = NP * DV;
     constexpr int BUF = TL * (6 * DK + 2 * DV + 4);  // q k la qc gy t1 | v g | scalars
     constexpr int GSP = DV + 1;                        // padded row of GS
-    static_assert(NT / 32 >= TL && TL == 8, "one warp per token of a chunk");
+    static_assert(NT / 32 == TL && TL == 8 && CW % 4 == 0, "one warp per token of a chunk");
     extern __shared__ float4 smem_f4[];
     float *sm = reinterpret_cast<float *>(smem_f4);
-    float *GS = sm + 2 * BUF;          // [DK][GSP]  dL/dS after the chunk's last token + 1
-    float *red_row = GS + DK * GSP;    // [TL][NT]   X v_u partials, by (x, part)
-    float *red_gk = red_row + TL * NT; // [TL][NT]   (GC + GC^T)_u k_u partials
-    float *red_col = red_gk + TL * NT; // [TL][NT]   X^T (P_u k_u) partials, by (y, vpart)
-    float *Lc = red_col + TL * NT;     // [TL][DK]   log P_u
-    float *kPt = Lc + TL * DK;         // [DK][TL]   P_u k_u, transposed
-    float *vt = kPt + DK * TL;         // [DV][TL]   v_u, transposed
-    float *gt = vt + DV * TL;          // [DV][TL]   g_u, transposed
-    float *gsvb = gt + DV * TL;        // [TL][DK]   GS_u v_u
-    float *Wv = gsvb + TL * DK;        // [TL][TL]   g_u' . v_u
-    float *Wk = Wv + TL * TL;          // [TL][TL]   sum_x P_u/P_u' qc_u' k_u
-    float *carry = Wk + TL * TL;       // [2][3][DK] acc, Gm, log alpha of the next token
-    const int tid = threadIdx.x, x = tid % DK, part = tid / DK, lane = tid & 31, warp = tid >> 5;
-    const int y = tid % DV, vpart = tid / DV;
+    float *GS = sm + 2 * BUF;           // [DK][GSP]   dL/dS after the chunk's last token + 1
+    float *red_row = GS + DK * GSP;     // [TL][NP][DK] X v_u partials
+    float *red_gk = red_row + TL * RED; // [TL][NP][DK] (GC + GC^T)_u k_u partials
+    float *red_col = red_gk + TL * RED; // [TL][NP][DV] X^T (P_u k_u) partials
+    float *Lc = red_col + TL * REDV;    // [TL][DK]    log P_u
+    float *kPt = Lc + TL * DK;          // [DK][TL]    P_u k_u, transposed
+    float *vt = kPt + DK * TL;          // [DV][TL]    v_u, transposed
+    float *gt = vt + DV * TL;           // [DV][TL]    g_u, transposed
+    float *gsvb = gt + DV * TL;         // [TL][DK]    GS_u v_u
+    float *Wv = gsvb + TL * DK;         // [TL][TL]    g_u' . v_u
+    float *Wk = Wv + TL * TL;           // [TL][TL]    sum_x P_u/P_u' qc_u' k_u
+    float *carry = Wk + TL * TL;        // [2][3][DK]  acc, Gm, log alpha of the next token
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int part = warp >> 1, half = warp & 1;
     const int bh = blockIdx.x, T = p.T;
     const size_t tok0 = (size_t)bh * T;
     const Ws ws(p, DK);
+    // row tile: rows xr(i) = half*DK/2 + lane + 32 i; column tile: columns
+    // yc(i) = half*DV/2 + lane + 32 i against rows part*RW ..
+    auto xr = [&](int i) { return half * (DK / 2) + lane + 32 * i; };
+    auto yc = [&](int i) { return half * (DV / 2) + lane + 32 * i; };
 
     for (int e = tid; e < DK * DV; e += NT)
         GS[(e / DV) * GSP + e % DV] = p.grad_S ? p.grad_S[(size_t)bh * DK * DV + e] : 0.f;
-    float Gr[RC];  // (GC + GC^T)[x][part*RC + r]
+    float Gr[RX][CW];  // (GC + GC^T)[xr(i)][part*CW + r]
 #pragma unroll
-    for (int r = 0; r < RC; ++r) {
-        const int j = part * RC + r;
-        Gr[r] = p.grad_C ? p.grad_C[((size_t)bh * DK + x) * DK + j] +
-                               p.grad_C[((size_t)bh * DK + j) * DK + x]
-                         : 0.f;
-    }
+    for (int i = 0; i < RX; ++i)
+#pragma unroll
+        for (int r = 0; r < CW; ++r) {
+            const int j = part * CW + r;
+            Gr[i][r] = p.grad_C ? p.grad_C[((size_t)bh * DK + xr(i)) * DK + j] +
+                                      p.grad_C[((size_t)bh * DK + j) * DK + xr(i)]
+                                : 0.f;
+        }
     if (tid < DK) {
-        carry[0 * DK + x] = ws.rs[(size_t)bh * DK + x];
-        carry[1 * DK + x] = p.grad_m ? p.grad_m[(size_t)bh * DK + x] : 0.f;
-        carry[2 * DK + x] = 0.f;
+        carry[0 * DK + tid] = ws.rs[(size_t)bh * DK + tid];
+        carry[1 * DK + tid] = p.grad_m ? p.grad_m[(size_t)bh * DK + tid] : 0.f;
+        carry[2 * DK + tid] = 0.f;
     }
     __syncthreads();
 
@@ -395,14 +449,14 @@ __global__ void __launch_bounds__(NT, 1) rev_sweep_kernel(const BwdParams p) {
         // (prep) log P_u = sum of log alpha over the tokens after u up to the
         // first token of the next chunk; P_u k_u, v and g transposed
         if (tid < DK) {
-            float s = cin[2 * DK + x];
+            float s = cin[2 * DK + tid];
             for (int u = TL - 1; u >= 0; --u) {
                 if (u < n) {
-                    Lc[u * DK + x] = s;
-                    kPt[x * TL + u] = expf(s) * K[u * DK + x];
-                    s += LA[u * DK + x];
+                    Lc[u * DK + tid] = s;
+                    kPt[tid * TL + u] = expf(s) * K[u * DK + tid];
+                    s += LA[u * DK + tid];
                 } else {
-                    kPt[x * TL + u] = 0.f;
+                    kPt[tid * TL + u] = 0.f;
                 }
             }
         } else if (tid < DK + DV) {
@@ -417,198 +471,235 @@ __global__ void __launch_bounds__(NT, 1) rev_sweep_kernel(const BwdParams p) {
 
         // (1a) rows of the entry state against every v_u
         {
-            float acc[TL];
+            float acc[RX][TL];
 #pragma unroll
-            for (int u = 0; u < TL; ++u) acc[u] = 0.f;
-            const float *row = GS + x * GSP + part * RS;
+            for (int i = 0; i < RX; ++i)
+#pragma unroll
+                for (int u = 0; u < TL; ++u) acc[i][u] = 0.f;
 #pragma unroll 4
-            for (int r = 0; r < RS; ++r) {
-                const float xv = row[r];
-                const float4 a = ld4(vt + (part * RS + r) * TL), c4 = ld4(vt + (part * RS + r) * TL + 4);
-                acc[0] = fmaf(xv, a.x, acc[0]);
-                acc[1] = fmaf(xv, a.y, acc[1]);
-                acc[2] = fmaf(xv, a.z, acc[2]);
-                acc[3] = fmaf(xv, a.w, acc[3]);
-                acc[4] = fmaf(xv, c4.x, acc[4]);
-                acc[5] = fmaf(xv, c4.y, acc[5]);
-                acc[6] = fmaf(xv, c4.z, acc[6]);
-                acc[7] = fmaf(xv, c4.w, acc[7]);
+            for (int r = 0; r < SW; ++r) {
+                const int d = part * SW + r;
+                const float4 a = ld4(vt + d * TL), c4 = ld4(vt + d * TL + 4);
+#pragma unroll
+                for (int i = 0; i < RX; ++i) {
+                    const float xv = GS[xr(i) * GSP + d];
+                    acc[i][0] = fmaf(xv, a.x, acc[i][0]);
+                    acc[i][1] = fmaf(xv, a.y, acc[i][1]);
+                    acc[i][2] = fmaf(xv, a.z, acc[i][2]);
+                    acc[i][3] = fmaf(xv, a.w, acc[i][3]);
+                    acc[i][4] = fmaf(xv, c4.x, acc[i][4]);
+                    acc[i][5] = fmaf(xv, c4.y, acc[i][5]);
+                    acc[i][6] = fmaf(xv, c4.z, acc[i][6]);
+                    acc[i][7] = fmaf(xv, c4.w, acc[i][7]);
+                }
             }
 #pragma unroll
-            for (int u = 0; u < TL; ++u) red_row[u * NT + part * DK + x] = acc[u];
+            for (int i = 0; i < RX; ++i)
+#pragma unroll
+                for (int u = 0; u < TL; ++u) red_row[u * RED + part * DK + xr(i)] = acc[i][u];
         }
         // (1b) columns of the entry state against every P_u k_u
         {
-            float acc[TL];
+            float acc[YX][TL];
 #pragma unroll
-            for (int u = 0; u < TL; ++u) acc[u] = 0.f;
+            for (int i = 0; i < YX; ++i)
+#pragma unroll
+                for (int u = 0; u < TL; ++u) acc[i][u] = 0.f;
 #pragma unroll 4
-            for (int r = 0; r < RV; ++r) {
-                const int xr = vpart * RV + r;
-                const float xv = GS[xr * GSP + y];
-                const float4 a = ld4(kPt + xr * TL), c4 = ld4(kPt + xr * TL + 4);
-                acc[0] = fmaf(xv, a.x, acc[0]);
-                acc[1] = fmaf(xv, a.y, acc[1]);
-                acc[2] = fmaf(xv, a.z, acc[2]);
-                acc[3] = fmaf(xv, a.w, acc[3]);
-                acc[4] = fmaf(xv, c4.x, acc[4]);
-                acc[5] = fmaf(xv, c4.y, acc[5]);
-                acc[6] = fmaf(xv, c4.z, acc[6]);
-                acc[7] = fmaf(xv, c4.w, acc[7]);
+            for (int r = 0; r < RW; ++r) {
+                const int x = part * RW + r;
+                const float4 a = ld4(kPt + x * TL), c4 = ld4(kPt + x * TL + 4);
+#pragma unroll
+                for (int i = 0; i < YX; ++i) {
+                    const float xv = GS[x * GSP + yc(i)];
+                    acc[i][0] = fmaf(xv, a.x, acc[i][0]);
+                    acc[i][1] = fmaf(xv, a.y, acc[i][1]);
+                    acc[i][2] = fmaf(xv, a.z, acc[i][2]);
+                    acc[i][3] = fmaf(xv, a.w, acc[i][3]);
+                    acc[i][4] = fmaf(xv, c4.x, acc[i][4]);
+                    acc[i][5] = fmaf(xv, c4.y, acc[i][5]);
+                    acc[i][6] = fmaf(xv, c4.z, acc[i][6]);
+                    acc[i][7] = fmaf(xv, c4.w, acc[i][7]);
+                }
             }
 #pragma unroll
-            for (int u = 0; u < TL; ++u) red_col[u * NT + vpart * DV + y] = acc[u];
+            for (int i = 0; i < YX; ++i)
+#pragma unroll
+                for (int u = 0; u < TL; ++u) red_col[u * REDV + part * DV + yc(i)] = acc[i][u];
         }
-        // (1c) the symmetric C adjoint, token by token backwards, on the owned rows
+        // (1c) the symmetric C adjoint, token by token backwards, on the tile
         for (int u = n - 1; u >= 0; --u) {
             const float rn = 1.0f / (float)(p.t0 + tc + u + 1);
-            const float gyn = GY[u * DK + x] * rn, qn = Q[u * DK + x] * rn;
             const float *qv = Q + u * DK, *yv = GY + u * DK, *kv = K + u * DK;
-            float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+            float gyn[RX], qn[RX], cc[RX];
 #pragma unroll
-            for (int r = 0; r < RC; r += 4) {
-                const float4 q4 = ld4(qv + part * RC + r), y4 = ld4(yv + part * RC + r);
-                const float4 k4 = ld4(kv + part * RC + r);
-                Gr[r] = fmaf(gyn, q4.x, fmaf(qn, y4.x, Gr[r]));
-                Gr[r + 1] = fmaf(gyn, q4.y, fmaf(qn, y4.y, Gr[r + 1]));
-                Gr[r + 2] = fmaf(gyn, q4.z, fmaf(qn, y4.z, Gr[r + 2]));
-                Gr[r + 3] = fmaf(gyn, q4.w, fmaf(qn, y4.w, Gr[r + 3]));
-                c0 = fmaf(Gr[r], k4.x, c0);
-                c1 = fmaf(Gr[r + 1], k4.y, c1);
-                c2 = fmaf(Gr[r + 2], k4.z, c2);
-                c3 = fmaf(Gr[r + 3], k4.w, c3);
+            for (int i = 0; i < RX; ++i) {
+                gyn[i] = yv[xr(i)] * rn;
+                qn[i] = qv[xr(i)] * rn;
+                cc[i] = 0.f;
             }
-            red_gk[u * NT + part * DK + x] = (c0 + c1) + (c2 + c3);
+#pragma unroll
+            for (int r = 0; r < CW; r += 4) {
+                const float4 q4 = ld4(qv + part * CW + r), y4 = ld4(yv + part * CW + r);
+                const float4 k4 = ld4(kv + part * CW + r);
+#pragma unroll
+                for (int i = 0; i < RX; ++i) {
+                    Gr[i][r] = fmaf(gyn[i], q4.x, fmaf(qn[i], y4.x, Gr[i][r]));
+                    Gr[i][r + 1] = fmaf(gyn[i], q4.y, fmaf(qn[i], y4.y, Gr[i][r + 1]));
+                    Gr[i][r + 2] = fmaf(gyn[i], q4.z, fmaf(qn[i], y4.z, Gr[i][r + 2]));
+                    Gr[i][r + 3] = fmaf(gyn[i], q4.w, fmaf(qn[i], y4.w, Gr[i][r + 3]));
+                    cc[i] = fmaf(Gr[i][r], k4.x, cc[i]);
+                    cc[i] = fmaf(Gr[i][r + 1], k4.y, cc[i]);
+                    cc[i] = fmaf(Gr[i][r + 2], k4.z, cc[i]);
+                    cc[i] = fmaf(Gr[i][r + 3], k4.w, cc[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < RX; ++i) red_gk[u * RED + part * DK + xr(i)] = cc[i];
         }
-        // (1d) warp u: the in-chunk pairs u' >= u
-        const int u = warp;
-        if (u < n) {
+        // (1d) the in-chunk pairs u <= u' (TL (TL + 1) / 2 of them), dealt
+        //      round-robin over the warps
+        for (int pr = warp; pr < TL * (TL + 1) / 2; pr += NT / 32) {
+            int up = 0, u = pr;
+            while (u > up) {
+                u -= up + 1;
+                ++up;
+            }
+            if (up >= n) continue;  // warp-uniform
+            float sv = 0.f, sk = 0.f;
 #pragma unroll
-            for (int up = 0; up < TL; ++up) {
-                if (up < u || up >= n) continue;  // warp-uniform
-                float sv = 0.f, sk = 0.f;
+            for (int i = 0; i < YL; ++i)
+                sv = fmaf(G[up * DV + lane + 32 * i], V[u * DV + lane + 32 * i], sv);
 #pragma unroll
-                for (int i = 0; i < YL; ++i)
-                    sv = fmaf(G[up * DV + lane + 32 * i], V[u * DV + lane + 32 * i], sv);
-#pragma unroll
-                for (int i = 0; i < XL; ++i) {
-                    const int xi = lane + 32 * i;
-                    const float rq = expf(Lc[u * DK + xi] - Lc[up * DK + xi]) * QC[up * DK + xi];
-                    sk = fmaf(rq, K[u * DK + xi], sk);
-                }
-                sv = warp_sum(sv);
-                sk = warp_sum(sk);
-                if (lane == 0) {
-                    Wv[up * TL + u] = sv;
-                    Wk[up * TL + u] = sk;
-                }
+            for (int i = 0; i < XL; ++i) {
+                const int xi = lane + 32 * i;
+                const float rq = expf(Lc[u * DK + xi] - Lc[up * DK + xi]) * QC[up * DK + xi];
+                sk = fmaf(rq, K[u * DK + xi], sk);
+            }
+            sv = warp_sum(sv);
+            sk = warp_sum(sk);
+            if (lane == 0) {
+                Wv[up * TL + u] = sv;
+                Wk[up * TL + u] = sk;
             }
         }
         __syncthreads();
 
-        // (2e) the state adjoint moves to the chunk's first token (owned rows)
+        // (2e) the state adjoint moves to the chunk's first token (the tile)
         {
-            float coef[TL];
-            const float l0 = n > 0 ? Lc[x] : 0.f;
+            float coef[RX][TL], e0[RX];
 #pragma unroll
-            for (int up = 0; up < TL; ++up)
-                coef[up] = up < n ? expf(l0 - Lc[up * DK + x]) * QC[up * DK + x] : 0.f;
-            const float e0 = expf(l0);
-            float *row = GS + x * GSP + part * RS;
+            for (int i = 0; i < RX; ++i) {
+                const float l0 = Lc[xr(i)];
+                e0[i] = expf(l0);
+#pragma unroll
+                for (int up = 0; up < TL; ++up)
+                    coef[i][up] =
+                        up < n ? expf(l0 - Lc[up * DK + xr(i)]) * QC[up * DK + xr(i)] : 0.f;
+            }
 #pragma unroll 4
-            for (int r = 0; r < RS; ++r) {
-                const float4 a = ld4(gt + (part * RS + r) * TL), c4 = ld4(gt + (part * RS + r) * TL + 4);
-                float g = e0 * row[r];
-                g = fmaf(coef[0], a.x, g);
-                g = fmaf(coef[1], a.y, g);
-                g = fmaf(coef[2], a.z, g);
-                g = fmaf(coef[3], a.w, g);
-                g = fmaf(coef[4], c4.x, g);
-                g = fmaf(coef[5], c4.y, g);
-                g = fmaf(coef[6], c4.z, g);
-                g = fmaf(coef[7], c4.w, g);
-                row[r] = g;
+            for (int r = 0; r < SW; ++r) {
+                const int d = part * SW + r;
+                const float4 a = ld4(gt + d * TL), c4 = ld4(gt + d * TL + 4);
+#pragma unroll
+                for (int i = 0; i < RX; ++i) {
+                    float *e = GS + xr(i) * GSP + d;
+                    float g = e0[i] * *e;
+                    g = fmaf(coef[i][0], a.x, g);
+                    g = fmaf(coef[i][1], a.y, g);
+                    g = fmaf(coef[i][2], a.z, g);
+                    g = fmaf(coef[i][3], a.w, g);
+                    g = fmaf(coef[i][4], c4.x, g);
+                    g = fmaf(coef[i][5], c4.y, g);
+                    g = fmaf(coef[i][6], c4.z, g);
+                    g = fmaf(coef[i][7], c4.w, g);
+                    *e = g;
+                }
             }
         }
-        // (2f) warp u: dk_u, dv_u and GS_u v_u
-        if (u < n) {
-            const long long t = tc + u;
+        // (2f) dk_u, GS_u v_u and dv_u.  Thread (x, a) takes the tokens
+        //      a, TL-1-a, a+NG, TL-1-a-NG, ... (NG = NT / DK groups), so every
+        //      thread sums over the same number of later tokens.
+        {
+            constexpr int NG = NT / DK, NGV = NT / DV;
+            const int x = tid % DK, a = tid / DK;
 #pragma unroll
-            for (int i = 0; i < XL; ++i) {
-                const int xi = lane + 32 * i;
+            for (int k2 = 0; k2 < TL / NG; ++k2) {
+                const int u = (k2 & 1) ? TL - 1 - a - (k2 >> 1) * NG : a + (k2 >> 1) * NG;
+                if (u >= n) continue;
                 float row = 0.f, gk = 0.f;
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
-                    row += red_row[u * NT + j * DK + xi];
-                    gk += red_gk[u * NT + j * DK + xi];
+                    row += red_row[u * RED + j * DK + x];
+                    gk += red_gk[u * RED + j * DK + x];
                 }
-                float gsv = expf(Lc[u * DK + xi]) * row;
-                float gm = cin[DK + xi];
-#pragma unroll
-                for (int up = 0; up < TL; ++up) {
-                    if (up < u || up >= n) continue;
-                    const float rq = expf(Lc[u * DK + xi] - Lc[up * DK + xi]) * QC[up * DK + xi];
-                    gsv = fmaf(rq, Wv[up * TL + u], gsv);
-                    gm -= GY[up * DK + xi] * SC[up * 4] + Q[up * DK + xi] * SC[up * 4 + 1];
+                const float lu = Lc[u * DK + x];
+                float gsv = expf(lu) * row, gm = cin[DK + x];
+                for (int up = u; up < n; ++up) {
+                    gsv = fmaf(expf(lu - Lc[up * DK + x]) * QC[up * DK + x], Wv[up * TL + u], gsv);
+                    gm -= GY[up * DK + x] * SC[up * 4] + Q[up * DK + x] * SC[up * 4 + 1];
                 }
-                gsvb[u * DK + xi] = gsv;
-                p.grad_k[(tok0 + t) * DK + xi] = gk + gm + gsv;
-                if (u == 0) cout[DK + xi] = gm;
+                gsvb[u * DK + x] = gsv;
+                p.grad_k[(tok0 + tc + u) * DK + x] = gk + gm + gsv;
+                if (u == 0) cout[DK + x] = gm;
             }
+            const int y = tid % DV, av = tid / DV;
 #pragma unroll
-            for (int i = 0; i < YL; ++i) {
-                const int yi = lane + 32 * i;
-                float s = 0.f;
+            for (int k2 = 0; k2 < TL / NGV; ++k2) {
+                const int u = (k2 & 1) ? TL - 1 - av - (k2 >> 1) * NGV : av + (k2 >> 1) * NGV;
+                if (u >= n) continue;
+                float s_ = 0.f;
 #pragma unroll
-                for (int j = 0; j < NPV; ++j) s += red_col[u * NT + j * DV + yi];
-                for (int up = u; up < n; ++up) s = fmaf(G[up * DV + yi], Wk[up * TL + u], s);
-                p.grad_v[(tok0 + t) * DV + yi] = s;
+                for (int j = 0; j < NP; ++j) s_ += red_col[u * REDV + j * DV + y];
+                for (int up = u; up < n; ++up) s_ = fmaf(G[up * DV + y], Wk[up * TL + u], s_);
+                p.grad_v[(tok0 + tc + u) * DV + y] = s_;
             }
         }
         __syncthreads();
 
-        // (3) warp u: the decay gradient, a suffix sum over the tokens
-        if (u < n) {
-            const long long t = tc + u;
-#pragma unroll
-            for (int i = 0; i < XL; ++i) {
-                const int xi = lane + 32 * i;
-                float a = cin[xi];
-                for (int up = u; up < n; ++up)
-                    a += T1[up * DK + xi] - K[up * DK + xi] * gsvb[up * DK + xi];
-                p.grad_la[(tok0 + t) * DK + xi] = a;
-                if (u == 0) {
-                    cout[xi] = a;
-                    cout[2 * DK + xi] = LA[xi];
-                }
+        // (3) the decay gradient: a suffix sum over the chunk, one thread per channel
+        if (tid < DK) {
+            float a = cin[tid];
+            for (int u = n - 1; u >= 0; --u) {
+                a += T1[u * DK + tid] - K[u * DK + tid] * gsvb[u * DK + tid];
+                p.grad_la[(tok0 + tc + u) * DK + tid] = a;
             }
+            cout[tid] = a;
+            cout[2 * DK + tid] = LA[tid];
         }
     }
     __syncthreads();
-    // gradients of the carried state (each thread writes what it owns)
+    // gradients of the carried state (each thread writes its own tiles)
     const float *cfin = carry + (it & 1) * 3 * DK;
-    if (p.grad_S0) {
-        const float a0 = expf(cfin[2 * DK + x]);
 #pragma unroll
-        for (int r = 0; r < RS; ++r)
-            p.grad_S0[((size_t)bh * DK + x) * DV + part * RS + r] = a0 * GS[x * GSP + part * RS + r];
-    }
-    if (p.grad_C0) {
+    for (int i = 0; i < RX; ++i) {
+        const size_t row = (size_t)bh * DK + xr(i);
+        if (p.grad_S0) {
+            const float a0 = expf(cfin[2 * DK + xr(i)]);
 #pragma unroll
-        for (int r = 0; r < RC; ++r)
-            p.grad_C0[((size_t)bh * DK + x) * DK + part * RC + r] = 0.5f * Gr[r];
+            for (int r = 0; r < SW; ++r)
+                p.grad_S0[row * DV + part * SW + r] = a0 * GS[xr(i) * GSP + part * SW + r];
+        }
+        if (p.grad_C0) {
+#pragma unroll
+            for (int r = 0; r < CW; ++r) p.grad_C0[row * DK + part * CW + r] = 0.5f * Gr[i][r];
+        }
     }
-    if (p.grad_m0 && tid < DK) p.grad_m0[(size_t)bh * DK + x] = cfin[DK + x];
+    if (p.grad_m0 && tid < DK) p.grad_m0[(size_t)bh * DK + tid] = cfin[DK + tid];
 }
 
-template <int DK, int DV, int NT = NT_F, int TL = TL_F>
+template <int DK, int DV>
 size_t fwd_smem() {
-    return sizeof(float) * (2 * (TL * (3 * DK + 2 * DV) + TL) + 3 * TL * NT + 2 * TL * DK + TL * TL);
+    constexpr int TL = TL_F, NP = NT_F / 32;
+    return sizeof(float) *
+           (2 * (TL * (3 * DK + 2 * DV) + TL) + 3 * TL * NP * DK + 2 * TL * DK + TL * TL);
 }
-template <int DK, int DV, int NT = NT_R, int TL = TL_R>
+template <int DK, int DV>
 size_t rev_smem() {
-    return sizeof(float) * (2 * TL * (6 * DK + 2 * DV + 4) + DK * (DV + 1) + 3 * TL * NT +
-                            TL * DK + DK * TL + 2 * DV * TL + TL * DK + 2 * TL * TL + 6 * DK);
+    constexpr int TL = TL_R, NP = 4;
+    return sizeof(float) * (2 * TL * (6 * DK + 2 * DV + 4) + DK * (DV + 1) +
+                            TL * NP * (2 * DK + DV) + TL * DK + DK * TL + 2 * DV * TL + TL * DK +
+                            2 * TL * TL + 6 * DK);
 }
 
 template <int DK, int DV>
