@@ -53,6 +53,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "sm103.cuh"
 
 namespace ccq {
 
@@ -363,49 +364,55 @@ __global__ void __launch_bounds__(NT_F, 1) fwd_sweep_kernel(const BwdParams p) {
 }
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
-    constexpr int NT = NT_R, TL = TL_R, NP = 4;   // 8 warps: 4 column slices x 2 row halves
-    constexpr int RX = DK / 64, CW = DK / NP, SW = DV / NP;   // row tiles of G and GS
-    constexpr int YX = DV / 64, RW = DK / NP;                // column tiles of the entry state
-    constexpr int XL = DK / 32, YL = DV / 32;
-    constexpr int RED = NP * DK, REDV = NP * DV;
-    constexpr int BUF = TL * (6 * DK + 2 * DV + 4);  // q k la qc gy t1 | v g | scalars
-    constexpr int GSP = DV + 1;                        // padded row of GS
-    static_assert(NT / 32 == TL && TL == 8 && CW % 4 == 0, "one warp per token of a chunk");
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT_R, 1)
+    rev_sweep_kernel(const BwdParams p) {
+    constexpr int NT = NT_R, TL = TL_R, NW = NT / 32;  // 8 warps, one per chunk token
+    constexpr int H2 = DK / 2;                          // rows of the adjoints this CTA owns
+    constexpr int RX = H2 / 32, CW = DK / NW, SW = DV / NW;  // row tiles: lanes x warps
+    constexpr int CG = DV / 32, RG = NW / CG, RW = H2 / RG;  // column tiles of the entry state
+    constexpr int XL = DK / 32, YL = DV / 32, DV2 = DV / 2;
+    constexpr int RED = NW * H2;                        // row partials per token
+    constexpr int COLP = 2 * RG;                        // column partials per (token, column)
+    constexpr int BUF = TL * (6 * DK + 2 * DV + 4);     // q k la qc gy t1 | v g | scalars
+    constexpr int GSP = DV + 1;                          // padded row of GS
+    static_assert(NW == TL && TL == 8 && CW % 4 == 0 && RX >= 1, "tile shapes");
     extern __shared__ float4 smem_f4[];
     float *sm = reinterpret_cast<float *>(smem_f4);
-    float *GS = sm + 2 * BUF;           // [DK][GSP]   dL/dS after the chunk's last token + 1
-    float *red_row = GS + DK * GSP;     // [TL][NP][DK] X v_u partials
-    float *red_gk = red_row + TL * RED; // [TL][NP][DK] (GC + GC^T)_u k_u partials
-    float *red_col = red_gk + TL * RED; // [TL][NP][DV] X^T (P_u k_u) partials
-    float *Lc = red_col + TL * REDV;    // [TL][DK]    log P_u
-    float *kPt = Lc + TL * DK;          // [DK][TL]    P_u k_u, transposed
-    float *vt = kPt + DK * TL;          // [DV][TL]    v_u, transposed
-    float *gt = vt + DV * TL;           // [DV][TL]    g_u, transposed
-    float *gsvb = gt + DV * TL;         // [TL][DK]    GS_u v_u
-    float *Wv = gsvb + TL * DK;         // [TL][TL]    g_u' . v_u
-    float *Wk = Wv + TL * TL;           // [TL][TL]    sum_x P_u/P_u' qc_u' k_u
-    float *carry = Wk + TL * TL;        // [2][3][DK]  acc, Gm, log alpha of the next token
+    float *GS = sm + 2 * BUF;            // [H2][GSP]   own rows of dL/dS after the chunk + 1
+    float *red_row = GS + H2 * GSP;      // [TL][NW][H2] X v_u partials
+    float *red_gk = red_row + TL * RED;  // [TL][NW][H2] (GC + GC^T)_u k_u partials
+    float *red_col = red_gk + TL * RED;  // [2][TL][COLP][DV2] X^T (P_u k_u), own columns
+    float *Lc = red_col + 2 * TL * COLP * DV2;  // [TL][DK]  log P_u
+    float *kPt = Lc + TL * DK;           // [DK][TL]    P_u k_u, transposed
+    float *vt = kPt + DK * TL;           // [DV][TL]    v_u, transposed
+    float *gt = vt + DV * TL;            // [DV][TL]    g_u, transposed
+    float *gsvb = gt + DV * TL;          // [TL][H2]    GS_u v_u (own rows)
+    float *Wv = gsvb + TL * H2;          // [TL][TL]    g_u' . v_u
+    float *Wk = Wv + TL * TL;            // [TL][TL]    sum_x P_u/P_u' qc_u' k_u
+    float *carry = Wk + TL * TL;         // [2][3][DK]  acc, Gm, log alpha of the next token
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int part = warp >> 1, half = warp & 1;
-    const int bh = blockIdx.x, T = p.T;
+    const int rank = (int)sm103::cluster_ctarank(), peer = rank ^ 1;
+    const int bh = blockIdx.x >> 1, T = p.T;
+    const int x0 = rank * H2;            // first row this CTA owns
     const size_t tok0 = (size_t)bh * T;
     const Ws ws(p, DK);
-    // row tile: rows xr(i) = half*DK/2 + lane + 32 i; column tile: columns
-    // yc(i) = half*DV/2 + lane + 32 i against rows part*RW ..
-    auto xr = [&](int i) { return half * (DK / 2) + lane + 32 * i; };
-    auto yc = [&](int i) { return half * (DV / 2) + lane + 32 * i; };
+    // row tile: local rows lane + 32 i, columns warp*CW .. (G) or warp*SW .. (GS)
+    // column tile: columns cg*32 + lane, local rows rg*RW .. (cg = warp % CG, rg = warp / CG)
+    const int cg = warp % CG, rg = warp / CG, ycol = cg * 32 + lane;
+    const uint32_t col_dst = sm103::mapa(
+        (uint32_t)__cvta_generic_to_shared(red_col), (ycol / DV2) == rank ? rank : peer);
 
-    for (int e = tid; e < DK * DV; e += NT)
-        GS[(e / DV) * GSP + e % DV] = p.grad_S ? p.grad_S[(size_t)bh * DK * DV + e] : 0.f;
-    float Gr[RX][CW];  // (GC + GC^T)[xr(i)][part*CW + r]
+    for (int e = tid; e < H2 * DV; e += NT)
+        GS[(e / DV) * GSP + e % DV] =
+            p.grad_S ? p.grad_S[((size_t)bh * DK + x0) * DV + e] : 0.f;
+    float Gr[RX][CW];  // (GC + GC^T)[x0 + lane + 32 i][warp*CW + r]
 #pragma unroll
     for (int i = 0; i < RX; ++i)
 #pragma unroll
         for (int r = 0; r < CW; ++r) {
-            const int j = part * CW + r;
-            Gr[i][r] = p.grad_C ? p.grad_C[((size_t)bh * DK + xr(i)) * DK + j] +
-                                      p.grad_C[((size_t)bh * DK + j) * DK + xr(i)]
+            const int x = x0 + lane + 32 * i, j = warp * CW + r;
+            Gr[i][r] = p.grad_C ? p.grad_C[((size_t)bh * DK + x) * DK + j] +
+                                      p.grad_C[((size_t)bh * DK + j) * DK + x]
                                 : 0.f;
         }
     if (tid < DK) {
@@ -413,7 +420,7 @@ __global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
         carry[1 * DK + tid] = p.grad_m ? p.grad_m[(size_t)bh * DK + tid] : 0.f;
         carry[2 * DK + tid] = 0.f;
     }
-    __syncthreads();
+    sm103::cluster_sync();  // both CTAs resident before any write into the peer's shared memory
 
     auto load = [&](int c) {
         float *b = sm + (c & 1) * BUF;
@@ -444,6 +451,7 @@ __global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
         const float *G = V + TL * DV, *SC = G + TL * DV;
         const float *cin = carry + (it & 1) * 3 * DK;
         float *cout = carry + ((it + 1) & 1) * 3 * DK;
+        const int par = it & 1;
         const int tc = c * TL, n = min(TL, T - tc);
 
         // (prep) log P_u = sum of log alpha over the tokens after u up to the
@@ -469,7 +477,7 @@ __global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
         }
         __syncthreads();
 
-        // (1a) rows of the entry state against every v_u
+        // (1a) own rows of the entry state against every v_u
         {
             float acc[RX][TL];
 #pragma unroll
@@ -478,11 +486,11 @@ __global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
                 for (int u = 0; u < TL; ++u) acc[i][u] = 0.f;
 #pragma unroll 4
             for (int r = 0; r < SW; ++r) {
-                const int d = part * SW + r;
+                const int d = warp * SW + r;
                 const float4 a = ld4(vt + d * TL), c4 = ld4(vt + d * TL + 4);
 #pragma unroll
                 for (int i = 0; i < RX; ++i) {
-                    const float xv = GS[xr(i) * GSP + d];
+                    const float xv = GS[(lane + 32 * i) * GSP + d];
                     acc[i][0] = fmaf(xv, a.x, acc[i][0]);
                     acc[i][1] = fmaf(xv, a.y, acc[i][1]);
                     acc[i][2] = fmaf(xv, a.z, acc[i][2]);
@@ -496,36 +504,36 @@ __global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
 #pragma unroll
             for (int i = 0; i < RX; ++i)
 #pragma unroll
-                for (int u = 0; u < TL; ++u) red_row[u * RED + part * DK + xr(i)] = acc[i][u];
+                for (int u = 0; u < TL; ++u) red_row[u * RED + warp * H2 + lane + 32 * i] = acc[i][u];
         }
-        // (1b) columns of the entry state against every P_u k_u
+        // (1b) columns of the entry state (own rows) against every P_u k_u; the
+        //      partial goes to the CTA that owns the column
         {
-            float acc[YX][TL];
+            float acc[TL];
 #pragma unroll
-            for (int i = 0; i < YX; ++i)
-#pragma unroll
-                for (int u = 0; u < TL; ++u) acc[i][u] = 0.f;
+            for (int u = 0; u < TL; ++u) acc[u] = 0.f;
 #pragma unroll 4
             for (int r = 0; r < RW; ++r) {
-                const int x = part * RW + r;
-                const float4 a = ld4(kPt + x * TL), c4 = ld4(kPt + x * TL + 4);
-#pragma unroll
-                for (int i = 0; i < YX; ++i) {
-                    const float xv = GS[x * GSP + yc(i)];
-                    acc[i][0] = fmaf(xv, a.x, acc[i][0]);
-                    acc[i][1] = fmaf(xv, a.y, acc[i][1]);
-                    acc[i][2] = fmaf(xv, a.z, acc[i][2]);
-                    acc[i][3] = fmaf(xv, a.w, acc[i][3]);
-                    acc[i][4] = fmaf(xv, c4.x, acc[i][4]);
-                    acc[i][5] = fmaf(xv, c4.y, acc[i][5]);
-                    acc[i][6] = fmaf(xv, c4.z, acc[i][6]);
-                    acc[i][7] = fmaf(xv, c4.w, acc[i][7]);
-                }
+                const int xl = rg * RW + r;
+                const float4 a = ld4(kPt + (x0 + xl) * TL), c4 = ld4(kPt + (x0 + xl) * TL + 4);
+                const float xv = GS[xl * GSP + ycol];
+                acc[0] = fmaf(xv, a.x, acc[0]);
+                acc[1] = fmaf(xv, a.y, acc[1]);
+                acc[2] = fmaf(xv, a.z, acc[2]);
+                acc[3] = fmaf(xv, a.w, acc[3]);
+                acc[4] = fmaf(xv, c4.x, acc[4]);
+                acc[5] = fmaf(xv, c4.y, acc[5]);
+                acc[6] = fmaf(xv, c4.z, acc[6]);
+                acc[7] = fmaf(xv, c4.w, acc[7]);
             }
+            const int slot = rg + RG * rank;  // partial index at the owner
 #pragma unroll
-            for (int i = 0; i < YX; ++i)
-#pragma unroll
-                for (int u = 0; u < TL; ++u) red_col[u * REDV + part * DV + yc(i)] = acc[i][u];
+            for (int u = 0; u < TL; ++u) {
+                const uint32_t off =
+                    (uint32_t)((((par * TL + u) * COLP + slot) * DV2 + ycol % DV2) * 4);
+                asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(col_dst + off), "f"(acc[u])
+                             : "memory");
+            }
         }
         // (1c) the symmetric C adjoint, token by token backwards, on the tile
         for (int u = n - 1; u >= 0; --u) {
@@ -534,14 +542,14 @@ __global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
             float gyn[RX], qn[RX], cc[RX];
 #pragma unroll
             for (int i = 0; i < RX; ++i) {
-                gyn[i] = yv[xr(i)] * rn;
-                qn[i] = qv[xr(i)] * rn;
+                gyn[i] = yv[x0 + lane + 32 * i] * rn;
+                qn[i] = qv[x0 + lane + 32 * i] * rn;
                 cc[i] = 0.f;
             }
 #pragma unroll
             for (int r = 0; r < CW; r += 4) {
-                const float4 q4 = ld4(qv + part * CW + r), y4 = ld4(yv + part * CW + r);
-                const float4 k4 = ld4(kv + part * CW + r);
+                const float4 q4 = ld4(qv + warp * CW + r), y4 = ld4(yv + warp * CW + r);
+                const float4 k4 = ld4(kv + warp * CW + r);
 #pragma unroll
                 for (int i = 0; i < RX; ++i) {
                     Gr[i][r] = fmaf(gyn[i], q4.x, fmaf(qn[i], y4.x, Gr[i][r]));
@@ -555,11 +563,11 @@ __global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
                 }
             }
 #pragma unroll
-            for (int i = 0; i < RX; ++i) red_gk[u * RED + part * DK + xr(i)] = cc[i];
+            for (int i = 0; i < RX; ++i) red_gk[u * RED + warp * H2 + lane + 32 * i] = cc[i];
         }
         // (1d) the in-chunk pairs u <= u' (TL (TL + 1) / 2 of them), dealt
-        //      round-robin over the warps
-        for (int pr = warp; pr < TL * (TL + 1) / 2; pr += NT / 32) {
+        //      round-robin over the warps (both CTAs form all of them)
+        for (int pr = warp; pr < TL * (TL + 1) / 2; pr += NW) {
             int up = 0, u = pr;
             while (u > up) {
                 u -= up + 1;
@@ -583,27 +591,27 @@ __global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
                 Wk[up * TL + u] = sk;
             }
         }
-        __syncthreads();
+        sm103::cluster_sync();  // the column partials of both CTAs have landed
 
-        // (2e) the state adjoint moves to the chunk's first token (the tile)
+        // (2e) the state adjoint moves to the chunk's first token (own tile)
         {
             float coef[RX][TL], e0[RX];
 #pragma unroll
             for (int i = 0; i < RX; ++i) {
-                const float l0 = Lc[xr(i)];
+                const int x = x0 + lane + 32 * i;
+                const float l0 = Lc[x];
                 e0[i] = expf(l0);
 #pragma unroll
                 for (int up = 0; up < TL; ++up)
-                    coef[i][up] =
-                        up < n ? expf(l0 - Lc[up * DK + xr(i)]) * QC[up * DK + xr(i)] : 0.f;
+                    coef[i][up] = up < n ? expf(l0 - Lc[up * DK + x]) * QC[up * DK + x] : 0.f;
             }
 #pragma unroll 4
             for (int r = 0; r < SW; ++r) {
-                const int d = part * SW + r;
+                const int d = warp * SW + r;
                 const float4 a = ld4(gt + d * TL), c4 = ld4(gt + d * TL + 4);
 #pragma unroll
                 for (int i = 0; i < RX; ++i) {
-                    float *e = GS + xr(i) * GSP + d;
+                    float *e = GS + (lane + 32 * i) * GSP + d;
                     float g = e0[i] * *e;
                     g = fmaf(coef[i][0], a.x, g);
                     g = fmaf(coef[i][1], a.y, g);
@@ -617,21 +625,21 @@ __global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
                 }
             }
         }
-        // (2f) dk_u, GS_u v_u and dv_u.  Thread (x, a) takes the tokens
-        //      a, TL-1-a, a+NG, TL-1-a-NG, ... (NG = NT / DK groups), so every
-        //      thread sums over the same number of later tokens.
+        // (2f) dk_u and GS_u v_u on own rows, dv_u on own columns.  Thread
+        //      (x, a) takes tokens a, TL-1-a, a+NG, ... so that every thread
+        //      sums over the same number of later tokens.
         {
-            constexpr int NG = NT / DK, NGV = NT / DV;
-            const int x = tid % DK, a = tid / DK;
+            constexpr int NG = NT / H2, NGV = NT / DV2;
+            const int xl = tid % H2, a = tid / H2, x = x0 + xl;
 #pragma unroll
-            for (int k2 = 0; k2 < TL / NG; ++k2) {
+            for (int k2 = 0; k2 < (TL + NG - 1) / NG; ++k2) {
                 const int u = (k2 & 1) ? TL - 1 - a - (k2 >> 1) * NG : a + (k2 >> 1) * NG;
                 if (u >= n) continue;
                 float row = 0.f, gk = 0.f;
 #pragma unroll
-                for (int j = 0; j < NP; ++j) {
-                    row += red_row[u * RED + j * DK + x];
-                    gk += red_gk[u * RED + j * DK + x];
+                for (int j = 0; j < NW; ++j) {
+                    row += red_row[u * RED + j * H2 + xl];
+                    gk += red_gk[u * RED + j * H2 + xl];
                 }
                 const float lu = Lc[u * DK + x];
                 float gsv = expf(lu) * row, gm = cin[DK + x];
@@ -639,53 +647,56 @@ __global__ void __launch_bounds__(NT_R, 1) rev_sweep_kernel(const BwdParams p) {
                     gsv = fmaf(expf(lu - Lc[up * DK + x]) * QC[up * DK + x], Wv[up * TL + u], gsv);
                     gm -= GY[up * DK + x] * SC[up * 4] + Q[up * DK + x] * SC[up * 4 + 1];
                 }
-                gsvb[u * DK + x] = gsv;
+                gsvb[u * H2 + xl] = gsv;
                 p.grad_k[(tok0 + tc + u) * DK + x] = gk + gm + gsv;
                 if (u == 0) cout[DK + x] = gm;
             }
-            const int y = tid % DV, av = tid / DV;
+            const int yl = tid % DV2, av = tid / DV2, y = rank * DV2 + yl;
 #pragma unroll
-            for (int k2 = 0; k2 < TL / NGV; ++k2) {
+            for (int k2 = 0; k2 < (TL + NGV - 1) / NGV; ++k2) {
                 const int u = (k2 & 1) ? TL - 1 - av - (k2 >> 1) * NGV : av + (k2 >> 1) * NGV;
                 if (u >= n) continue;
                 float s_ = 0.f;
 #pragma unroll
-                for (int j = 0; j < NP; ++j) s_ += red_col[u * REDV + j * DV + y];
+                for (int j = 0; j < COLP; ++j) s_ += red_col[((par * TL + u) * COLP + j) * DV2 + yl];
                 for (int up = u; up < n; ++up) s_ = fmaf(G[up * DV + y], Wk[up * TL + u], s_);
                 p.grad_v[(tok0 + tc + u) * DV + y] = s_;
             }
         }
         __syncthreads();
 
-        // (3) the decay gradient: a suffix sum over the chunk, one thread per channel
-        if (tid < DK) {
-            float a = cin[tid];
+        // (3) the decay gradient: a suffix sum over the chunk, one thread per
+        //     own channel; the next chunk's decay reference for every channel
+        if (tid < H2) {
+            const int x = x0 + tid;
+            float a = cin[x];
             for (int u = n - 1; u >= 0; --u) {
-                a += T1[u * DK + tid] - K[u * DK + tid] * gsvb[u * DK + tid];
-                p.grad_la[(tok0 + tc + u) * DK + tid] = a;
+                a += T1[u * DK + x] - K[u * DK + x] * gsvb[u * H2 + tid];
+                p.grad_la[(tok0 + tc + u) * DK + x] = a;
             }
-            cout[tid] = a;
-            cout[2 * DK + tid] = LA[tid];
+            cout[x] = a;
         }
+        if (tid < DK) cout[2 * DK + tid] = LA[tid];
     }
     __syncthreads();
-    // gradients of the carried state (each thread writes its own tiles)
+    // gradients of the carried state (own rows; each thread writes its tiles)
     const float *cfin = carry + (it & 1) * 3 * DK;
 #pragma unroll
     for (int i = 0; i < RX; ++i) {
-        const size_t row = (size_t)bh * DK + xr(i);
+        const int x = x0 + lane + 32 * i;
+        const size_t row = (size_t)bh * DK + x;
         if (p.grad_S0) {
-            const float a0 = expf(cfin[2 * DK + xr(i)]);
+            const float a0 = expf(cfin[2 * DK + x]);
 #pragma unroll
             for (int r = 0; r < SW; ++r)
-                p.grad_S0[row * DV + part * SW + r] = a0 * GS[xr(i) * GSP + part * SW + r];
+                p.grad_S0[row * DV + warp * SW + r] = a0 * GS[(lane + 32 * i) * GSP + warp * SW + r];
         }
         if (p.grad_C0) {
 #pragma unroll
-            for (int r = 0; r < CW; ++r) p.grad_C0[row * DK + part * CW + r] = 0.5f * Gr[i][r];
+            for (int r = 0; r < CW; ++r) p.grad_C0[row * DK + warp * CW + r] = 0.5f * Gr[i][r];
         }
     }
-    if (p.grad_m0 && tid < DK) p.grad_m0[(size_t)bh * DK + tid] = cfin[DK + tid];
+    if (p.grad_m0 && tid < H2) p.grad_m0[(size_t)bh * DK + x0 + tid] = cfin[DK + x0 + tid];
 }
 
 template <int DK, int DV>
@@ -696,10 +707,10 @@ size_t fwd_smem() {
 }
 template <int DK, int DV>
 size_t rev_smem() {
-    constexpr int TL = TL_R, NP = 4;
-    return sizeof(float) * (2 * TL * (6 * DK + 2 * DV + 4) + DK * (DV + 1) +
-                            TL * NP * (2 * DK + DV) + TL * DK + DK * TL + 2 * DV * TL + TL * DK +
-                            2 * TL * TL + 6 * DK);
+    constexpr int TL = TL_R, NW = NT_R / 32, H2 = DK / 2, RG = NW / (DV / 32);
+    return sizeof(float) * (2 * TL * (6 * DK + 2 * DV + 4) + H2 * (DV + 1) + 2 * TL * NW * H2 +
+                            2 * TL * (2 * RG) * (DV / 2) + TL * DK + DK * TL + 2 * DV * TL +
+                            TL * H2 + 2 * TL * TL + 6 * DK);
 }
 
 template <int DK, int DV>
@@ -714,7 +725,7 @@ cudaError_t launch_shape(const BwdParams &p, cudaStream_t st) {
     fwd_sweep_kernel<DK, DV><<<p.BH, NT_F, fb, st>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    rev_sweep_kernel<DK, DV><<<p.BH, NT_R, rb, st>>>(p);
+    rev_sweep_kernel<DK, DV><<<2 * p.BH, NT_R, rb, st>>>(p);  // a CTA pair per (b, h)
     return cudaGetLastError();
 }
 
