@@ -9,24 +9,28 @@
 //   lambda_t = sigmoid(w . q_t + b)  (or given),  qc_t = q_t - lambda_t y_t,
 //   o_t = S_t^T qc_t.
 //
-// Two sweeps over the tokens, one CTA per (b, h) in each, chunks of TL = 8
-// tokens with one warp per token of a chunk:
+// Two sweeps over the tokens, each run by a pair of CTAs (a thread-block
+// cluster) per (b, h), in chunks of TL = 8 tokens with one warp per token of
+// a chunk.  Each CTA of a pair owns half of the rows of the state matrices;
+// what crosses between them goes through distributed shared memory.
 //
 // 1. Forward sweep.  Everything that depends on the forward state can be
 //    formed going forward, because the upstream gradient g_t = dL/do_t is
 //    known: gqc_t = S_t g_t, glambda_t = -y_t . gqc_t, gy_t = -lambda_t gqc_t,
 //    and the query gradient
 //      dq_t = gqc_t + Sigma_t gy_t + lambda_t (1 - lambda_t) glambda_t w.
-//    C and S stay in registers: thread (x, part) owns row x of C and row x
-//    of S, each over one slice of columns, the only elements it ever reads
-//    or writes (C is symmetric, so C0 must be too: it is a sum of k k^T).
+//    C and S stay in registers: thread (lane, warp) owns a tile of rows
+//    (lane + 32 i of its CTA's half) by one column slice (per warp) of C and
+//    of S, the only elements it ever reads or writes (C is symmetric, so C0
+//    must be too: it is a sum of k k^T).
 //    Per chunk: (A) every thread applies the chunk's writes token by token
-//    to its rows and leaves the partial products C_u q_u and S_u g_u;
-//    (B) warp u finishes token u's read and local gradients; (C) the
-//    products C_end gy_u with the chunk's last C, corrected in (D) by
-//    - sum_{u'>u} k_u' (k_u' . gy_u) to C_u gy_u.  Four block barriers per
-//    chunk.  Per token it leaves in the workspace qc_t, gy_t, qc_t * gqc_t
-//    and the two scalars (mu.q)/n and (mu.gy)/n that rebuild dL/dmu_t / n_t.
+//    to its tiles and leaves the partial products C_u q_u and S_u g_u;
+//    (B) warp u finishes token u's read and local gradients on the CTA's
+//    channels, exchanging with the peer the halves of m.q, w.q, y.gqc, mu.gy
+//    and of gy_u; (C) the products C_end gy_u with the chunk's last C,
+//    corrected in (D) by - sum_{u'>u} k_u' (k_u' . gy_u) to C_u gy_u.
+//    Per token it leaves in the workspace qc_t, gy_t, qc_t * gqc_t and the
+//    two scalars (mu.q)/n and (mu.gy)/n that rebuild dL/dmu_t / n_t.
 //
 // 2. Reverse sweep.  The adjoints of the three sums run backwards:
 //      GS_t = qc_t g_t^T + Diag(alpha_{t+1}) GS_{t+1}      (dL/dS_t)
@@ -34,20 +38,21 @@
 //      Gm_t = dL/dmu_t / n_t + Gm_{t+1}                    (dL/dm_t)
 //    with dk_t = (GC_t + GC_t^T) k_t + Gm_t + GS_t v_t and dv_t = GS_t^T k_t.
 //    GC enters only through GC + GC^T, so that symmetric sum is what is kept
-//    (registers, row-owned, updated token by token).  GS sits in shared
-//    memory with padded rows and moves a chunk at a time: inside a chunk,
-//    with X the adjoint entering it and P_u the decay product from token u
-//    to the chunk's end,
+//    (registers, row tiles, updated token by token).  Each CTA keeps its half
+//    of the rows of GS in shared memory (padded rows) and moves it a chunk at
+//    a time; the column products GS^T k of its rows go to the CTA that owns
+//    those columns of dv.  Inside a chunk, with X the adjoint entering it
+//    and P_u the decay product from token u to the chunk's end,
 //      GS_u = P_u X + sum_{u' >= u} (P_u / P_u') qc_u' g_u'^T,
 //    so GS_u v_u and GS_u^T k_u are one pass over the rows and one over the
 //    columns of X against all eight tokens, plus 8 x 8 in-chunk terms.
 //    The decay gradient uses d log A_t = qc_t * gqc_t - k_t * (GS_t v_t)
 //    (A_t the running product of alpha; the final state adds
 //    rowsum(dL/dS_T * S_T)), summed over t' >= t: no sweep ever needs
-//    S_{t-1}, and no state is rebuilt by dividing out a decay.  Five block
-//    barriers per chunk.
+//    S_{t-1}, and no state is rebuilt by dividing out a decay.
 //
-// Shapes: dk, dv in {64, 128}; any T (a ragged last chunk); 256 threads.
+// Shapes: dk, dv in {64, 128}; any T (a ragged last chunk); 256 threads per
+// CTA, 2 B H CTAs per sweep.
 // Token vectors are staged a chunk at a time with cp.async (16-byte
 // copies, double-buffered) so each chunk's loads overlap the previous chunk.
 #include <mutex>
@@ -96,47 +101,53 @@ struct Ws {
 };
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(NT_F, 1) fwd_sweep_kernel(const BwdParams p) {
-    constexpr int NT = NT_F, TL = TL_F, NP = NT / 32;  // 8 warps = 8 column slices
-    constexpr int RX = DK / 32, CW = DK / NP, SW = DV / NP, XL = DK / 32;
-    constexpr int RED = NP * DK;                       // partial products per token
-    constexpr int BUF = TL * (3 * DK + 2 * DV) + TL;   // q k la | v g | lambda
-    static_assert(NP == TL && CW % 4 == 0 && SW % 4 == 0, "one warp per token of a chunk");
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT_F, 1)
+    fwd_sweep_kernel(const BwdParams p) {
+    constexpr int NT = NT_F, TL = TL_F, NW = NT / 32;  // 8 warps, one per chunk token
+    constexpr int H2 = DK / 2;                          // rows of C and S this CTA owns
+    constexpr int RX = H2 / 32, CW = DK / NW, SW = DV / NW;
+    constexpr int RED = NW * H2;                        // partial products per token
+    constexpr int BUF = TL * (3 * DK + 2 * DV) + TL;    // q k la | v g | lambda
+    static_assert(NW == TL && CW % 4 == 0 && SW % 4 == 0 && RX >= 1, "tile shapes");
     extern __shared__ float4 smem_f4[];
     float *sm = reinterpret_cast<float *>(smem_f4);
-    float *red1 = sm + 2 * BUF;     // [TL][NP][DK]  C_u q_u partials
-    float *red2 = red1 + TL * RED;  // [TL][NP][DK]  S_u g_u partials
-    float *red3 = red2 + TL * RED;  // [TL][NP][DK]  C_end gy_u partials
-    float *mb = red3 + TL * RED;    // [TL][DK]      m after token u
-    float *gyb = mb + TL * DK;      // [TL][DK]      gy_u
+    float *red1 = sm + 2 * BUF;     // [TL][NW][H2]  C_u q_u partials (own rows)
+    float *red2 = red1 + TL * RED;  // [TL][NW][H2]  S_u g_u partials
+    float *red3 = red2 + TL * RED;  // [TL][NW][H2]  C_end gy_u partials
+    float *mb = red3 + TL * RED;    // [TL][H2]      m after token u (own channels)
+    float *gyb = mb + TL * H2;      // [TL][DK]      gy_u, both halves
     float *dmat = gyb + TL * DK;    // [TL][TL]      k_u' . gy_u (u' > u)
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, part = warp;
-    const int bh = blockIdx.x, h = bh % p.H, T = p.T;
+    float *xch = dmat + TL * TL;    // [2][TL][4]    per-CTA halves of m.q, w.q, y.gqc, mu.gy
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int rank = (int)sm103::cluster_ctarank(), peer = rank ^ 1;
+    const int bh = blockIdx.x >> 1, h = bh % p.H, T = p.T;
+    const int x0 = rank * H2;
     const size_t tok0 = (size_t)bh * T;
     const Ws ws(p, DK);
     const bool gate = p.lambda_in == nullptr;
+    const uint32_t gyb_peer = sm103::mapa((uint32_t)__cvta_generic_to_shared(gyb), peer);
+    const uint32_t xch_peer = sm103::mapa((uint32_t)__cvta_generic_to_shared(xch), peer);
 
-    // thread tile: rows x_i = lane + 32 i of C (columns part*CW ..) and of S
-    // (columns part*SW ..)
+    // thread tile: own rows x0 + lane + 32 i of C (columns warp*CW ..) and of
+    // S (columns warp*SW ..); the same lanes carry those channels in the
+    // warp-per-token phases
     float Cr[RX][CW], Sr[RX][SW];
+    float m_r[RX], wl[RX], dw[RX];
 #pragma unroll
     for (int i = 0; i < RX; ++i) {
-        const size_t row = (size_t)bh * DK + lane + 32 * i;
+        const int x = x0 + lane + 32 * i;
+        const size_t row = (size_t)bh * DK + x;
 #pragma unroll
-        for (int r = 0; r < CW; ++r) Cr[i][r] = p.C0 ? p.C0[row * DK + part * CW + r] : 0.f;
+        for (int r = 0; r < CW; ++r) Cr[i][r] = p.C0 ? p.C0[row * DK + warp * CW + r] : 0.f;
 #pragma unroll
-        for (int r = 0; r < SW; ++r) Sr[i][r] = p.S0 ? p.S0[row * DV + part * SW + r] : 0.f;
-    }
-    // the same lanes carry channel x = lane + 32 i in the warp-per-token phases
-    float m_r[RX], wl[XL], dw[XL];
-#pragma unroll
-    for (int i = 0; i < XL; ++i) {
-        m_r[i] = (part == 0 && p.m0) ? p.m0[(size_t)bh * DK + lane + 32 * i] : 0.f;
-        wl[i] = gate ? p.w_lambda[h * DK + lane + 32 * i] : 0.f;
+        for (int r = 0; r < SW; ++r) Sr[i][r] = p.S0 ? p.S0[row * DV + warp * SW + r] : 0.f;
+        m_r[i] = (warp == 0 && p.m0) ? p.m0[row] : 0.f;
+        wl[i] = gate ? p.w_lambda[h * DK + x] : 0.f;
         dw[i] = 0.f;
     }
     const float bl = gate ? p.b_lambda[h] : 0.f;
     float db = 0.f;
+    sm103::cluster_sync();  // both CTAs resident before any write into the peer's shared memory
 
     auto load = [&](int c) {
         float *b = sm + (c & 1) * BUF;
@@ -149,6 +160,13 @@ __global__ void __launch_bounds__(NT_F, 1) fwd_sweep_kernel(const BwdParams p) {
         stage<NT>(b + 3 * TL * DK + TL * DV, p.grad_o + r0 * DV, n * DV);
         if (!gate && tid < n) b[3 * TL * DK + 2 * TL * DV + tid] = p.lambda_in[r0 + tid];
         cp_commit();
+    };
+    // a float written to this CTA's copy and to the peer's copy of an array
+    auto put2 = [&](float *local, uint32_t peer_base, int idx, float v) {
+        local[idx] = v;
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(peer_base + 4u * (uint32_t)idx),
+                     "f"(v)
+                     : "memory");
     };
 
     const int nch = (T + TL - 1) / TL;
@@ -170,14 +188,14 @@ __global__ void __launch_bounds__(NT_F, 1) fwd_sweep_kernel(const BwdParams p) {
             float kx[RX], ax[RX], a[RX], s[RX];
 #pragma unroll
             for (int i = 0; i < RX; ++i) {
-                kx[i] = kv[lane + 32 * i];
-                ax[i] = expf(LA[u * DK + lane + 32 * i]);
+                kx[i] = kv[x0 + lane + 32 * i];
+                ax[i] = expf(LA[u * DK + x0 + lane + 32 * i]);
                 a[i] = 0.f;
                 s[i] = 0.f;
             }
 #pragma unroll
             for (int r = 0; r < CW; r += 4) {
-                const float4 k4 = ld4(kv + part * CW + r), q4 = ld4(qv + part * CW + r);
+                const float4 k4 = ld4(kv + warp * CW + r), q4 = ld4(qv + warp * CW + r);
 #pragma unroll
                 for (int i = 0; i < RX; ++i) {
                     Cr[i][r] = fmaf(k4.x, kx[i], Cr[i][r]);
@@ -192,7 +210,7 @@ __global__ void __launch_bounds__(NT_F, 1) fwd_sweep_kernel(const BwdParams p) {
             }
 #pragma unroll
             for (int r = 0; r < SW; r += 4) {
-                const float4 v4 = ld4(vv + part * SW + r), g4 = ld4(gv + part * SW + r);
+                const float4 v4 = ld4(vv + warp * SW + r), g4 = ld4(gv + warp * SW + r);
 #pragma unroll
                 for (int i = 0; i < RX; ++i) {
                     Sr[i][r] = fmaf(ax[i], Sr[i][r], kx[i] * v4.x);
@@ -207,70 +225,87 @@ __global__ void __launch_bounds__(NT_F, 1) fwd_sweep_kernel(const BwdParams p) {
             }
 #pragma unroll
             for (int i = 0; i < RX; ++i) {
-                red1[u * RED + part * DK + lane + 32 * i] = a[i];
-                red2[u * RED + part * DK + lane + 32 * i] = s[i];
+                red1[u * RED + warp * H2 + lane + 32 * i] = a[i];
+                red2[u * RED + warp * H2 + lane + 32 * i] = s[i];
             }
-            if (part == 0) {
+            if (warp == 0) {
 #pragma unroll
                 for (int i = 0; i < RX; ++i) {
                     m_r[i] += kx[i];
-                    mb[u * DK + lane + 32 * i] = m_r[i];
+                    mb[u * H2 + lane + 32 * i] = m_r[i];
                 }
             }
         }
         __syncthreads();
 
-        // (B) warp u: the read and the local gradients of token u
+        // (B1) warp u: C_u q_u, S_u g_u on own channels; this CTA's halves of
+        //      m.q and w.q go to both CTAs
         const int u = warp;
         const long long t = tc + u;
-        float gqc[XL], qc[XL], gy[XL], mu[XL];
-        float rn = 0.f, mqn = 0.f, lam = 0.f, gl = 0.f, mg = 0.f;
+        float cq[RX], gqc[RX];
         if (u < n) {
             const float *qv = Q + u * DK;
-            float cq[XL], mq = 0.f, z = 0.f;
+            float mq = 0.f, z = 0.f;
 #pragma unroll
-            for (int i = 0; i < XL; ++i) {
-                const int xi = lane + 32 * i;
+            for (int i = 0; i < RX; ++i) {
+                const int xl = lane + 32 * i;
                 cq[i] = 0.f;
                 gqc[i] = 0.f;
 #pragma unroll
-                for (int j = 0; j < NP; ++j) {
-                    cq[i] += red1[u * RED + j * DK + xi];
-                    gqc[i] += red2[u * RED + j * DK + xi];
+                for (int j = 0; j < NW; ++j) {
+                    cq[i] += red1[u * RED + j * H2 + xl];
+                    gqc[i] += red2[u * RED + j * H2 + xl];
                 }
-                mq = fmaf(mb[u * DK + xi], qv[xi], mq);
-                z = fmaf(wl[i], qv[xi], z);
+                mq = fmaf(mb[u * H2 + xl], qv[x0 + xl], mq);
+                z = fmaf(wl[i], qv[x0 + xl], z);
             }
             mq = warp_sum(mq);
             z = warp_sum(z);
+            if (lane == 0) put2(xch, xch_peer, (rank * TL + u) * 4 + 0, mq);
+            if (lane == 1) put2(xch, xch_peer, (rank * TL + u) * 4 + 1, z);
+        }
+        sm103::cluster_sync();
+
+        // (B2) warp u: the read and the local gradients of token u on own
+        //      channels; gy_u to both CTAs, halves of y.gqc and mu.gy too
+        float qc[RX], gy[RX], mu[RX];
+        float rn = 0.f, mqn = 0.f, lam = 0.f;
+        if (u < n) {
+            const float *qv = Q + u * DK;
+            const float mq = xch[u * 4] + xch[(TL + u) * 4];
+            const float z = xch[u * 4 + 1] + xch[(TL + u) * 4 + 1];
             rn = 1.0f / (float)(p.t0 + t + 1);
             mqn = mq * rn;  // mu . q
             lam = gate ? 1.0f / (1.0f + expf(-(z + bl))) : LAM[u];
             float glp = 0.f, mgp = 0.f;
 #pragma unroll
-            for (int i = 0; i < XL; ++i) {
-                const int xi = lane + 32 * i;
-                mu[i] = mb[u * DK + xi] * rn;
+            for (int i = 0; i < RX; ++i) {
+                const int xl = lane + 32 * i;
+                mu[i] = mb[u * H2 + xl] * rn;
                 const float y = cq[i] * rn - mu[i] * mqn;
-                qc[i] = qv[xi] - lam * y;
+                qc[i] = qv[x0 + xl] - lam * y;
                 gy[i] = -lam * gqc[i];
-                gyb[u * DK + xi] = gy[i];
+                put2(gyb, gyb_peer, u * DK + x0 + xl, gy[i]);
                 glp = fmaf(-y, gqc[i], glp);
                 mgp = fmaf(mu[i], gy[i], mgp);
             }
-            gl = warp_sum(glp);
-            mg = warp_sum(mgp);
+            glp = warp_sum(glp);
+            mgp = warp_sum(mgp);
+            if (lane == 0) put2(xch, xch_peer, (rank * TL + u) * 4 + 2, glp);
+            if (lane == 1) put2(xch, xch_peer, (rank * TL + u) * 4 + 3, mgp);
         }
-        __syncthreads();
+        sm103::cluster_sync();
 
-        // (C) C_end gy_u for every token, on the thread's tile of C
+        // (C) C_end gy_u for every token on the thread's tile of C, and
+        //     k_u' . gy_u for u < u' (C_u = C_end - sum_{u'>u} k_u' k_u'^T),
+        //     those pairs dealt round-robin over the warps
         for (int v_ = 0; v_ < n; ++v_) {
             float a[RX];
 #pragma unroll
             for (int i = 0; i < RX; ++i) a[i] = 0.f;
 #pragma unroll
             for (int r = 0; r < CW; r += 4) {
-                const float4 y4 = ld4(gyb + v_ * DK + part * CW + r);
+                const float4 y4 = ld4(gyb + v_ * DK + warp * CW + r);
 #pragma unroll
                 for (int i = 0; i < RX; ++i) {
                     a[i] = fmaf(Cr[i][r], y4.x, a[i]);
@@ -280,11 +315,9 @@ __global__ void __launch_bounds__(NT_F, 1) fwd_sweep_kernel(const BwdParams p) {
                 }
             }
 #pragma unroll
-            for (int i = 0; i < RX; ++i) red3[v_ * RED + part * DK + lane + 32 * i] = a[i];
+            for (int i = 0; i < RX; ++i) red3[v_ * RED + warp * H2 + lane + 32 * i] = a[i];
         }
-        // k_u' . gy_u for u < u' (C_u = C_end - sum_{u'>u} k_u' k_u'^T), the
-        // TL (TL - 1) / 2 pairs dealt round-robin over the warps
-        for (int pr = warp; pr < TL * (TL - 1) / 2; pr += NT / 32) {
+        for (int pr = warp; pr < TL * (TL - 1) / 2; pr += NW) {
             int up = 1, uu = pr;
             while (uu >= up) {
                 uu -= up;
@@ -293,71 +326,73 @@ __global__ void __launch_bounds__(NT_F, 1) fwd_sweep_kernel(const BwdParams p) {
             if (up >= n) continue;  // warp-uniform
             float s_ = 0.f;
 #pragma unroll
-            for (int i = 0; i < XL; ++i)
+            for (int i = 0; i < DK / 32; ++i)
                 s_ = fmaf(K[up * DK + lane + 32 * i], gyb[uu * DK + lane + 32 * i], s_);
             s_ = warp_sum(s_);
             if (lane == 0) dmat[up * TL + uu] = s_;
         }
         __syncthreads();
 
-        // (D) warp u: dq_u and what the reverse sweep needs
+        // (D) warp u: dq_u on own channels and what the reverse sweep needs
         if (u < n) {
+            const float gl = xch[u * 4 + 2] + xch[(TL + u) * 4 + 2];
+            const float mg = xch[u * 4 + 3] + xch[(TL + u) * 4 + 3];
             const float gz = gate ? gl * lam * (1.0f - lam) : 0.f;
             const float *qv = Q + u * DK;
 #pragma unroll
-            for (int i = 0; i < XL; ++i) {
-                const int xi = lane + 32 * i;
+            for (int i = 0; i < RX; ++i) {
+                const int xl = lane + 32 * i, x = x0 + xl;
                 float cgy = 0.f;
 #pragma unroll
-                for (int j = 0; j < NP; ++j) cgy += red3[u * RED + j * DK + xi];
-                for (int up = u + 1; up < n; ++up) cgy -= K[up * DK + xi] * dmat[up * TL + u];
-                const size_t o = (tok0 + t) * DK + xi;
+                for (int j = 0; j < NW; ++j) cgy += red3[u * RED + j * H2 + xl];
+                for (int up = u + 1; up < n; ++up) cgy -= K[up * DK + x] * dmat[up * TL + u];
+                const size_t o = (tok0 + t) * DK + x;
                 p.grad_q[o] = gqc[i] + (cgy * rn - mu[i] * mg) + gz * wl[i];
                 ws.qc[o] = qc[i];
                 ws.gy[o] = gy[i];
                 ws.t1[o] = qc[i] * gqc[i];
-                dw[i] = fmaf(gz, qv[xi], dw[i]);
+                dw[i] = fmaf(gz, qv[x], dw[i]);
             }
-            if (lane == 0) {
+            if (lane == 0 && rank == 0) {
                 *reinterpret_cast<float4 *>(ws.sc + (tok0 + t) * 4) =
                     make_float4(mqn * rn, mg * rn, 0.f, 0.f);
                 db += gz;
             }
         }
     }
-    // rowsum(dL/dS_T * S_T): the final state's share of the decay gradient;
-    // the gate gradients summed over the warps
+    // rowsum(dL/dS_T * S_T) on own rows: the final state's share of the decay
+    // gradient; the gate gradients summed over the warps
     float rs[RX];
 #pragma unroll
     for (int i = 0; i < RX; ++i) {
         rs[i] = 0.f;
         if (p.grad_S) {
-            const size_t row = (size_t)bh * DK + lane + 32 * i;
+            const size_t row = (size_t)bh * DK + x0 + lane + 32 * i;
 #pragma unroll
             for (int r = 0; r < SW; ++r)
-                rs[i] = fmaf(p.grad_S[row * DV + part * SW + r], Sr[i][r], rs[i]);
+                rs[i] = fmaf(p.grad_S[row * DV + warp * SW + r], Sr[i][r], rs[i]);
         }
     }
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < RX; ++i) {
-        red1[part * DK + lane + 32 * i] = rs[i];
-        red2[warp * DK + lane + 32 * i] = dw[i];
+        red1[warp * H2 + lane + 32 * i] = rs[i];
+        red2[warp * H2 + lane + 32 * i] = dw[i];
     }
-    if (lane == 0) red2[TL * DK + warp] = db;
+    if (lane == 0) red3[warp] = db;
     __syncthreads();
-    if (tid < DK) {
+    if (tid < H2) {
         float s = 0.f, w_ = 0.f;
 #pragma unroll
-        for (int j = 0; j < NP; ++j) {
-            s += red1[j * DK + tid];
-            w_ += red2[j * DK + tid];
+        for (int j = 0; j < NW; ++j) {
+            s += red1[j * H2 + tid];
+            w_ += red2[j * H2 + tid];
         }
-        ws.rs[(size_t)bh * DK + tid] = s;
-        if (p.grad_w) p.grad_w[(size_t)bh * DK + tid] = w_;
-        if (p.grad_b && tid == 0) {
+        ws.rs[(size_t)bh * DK + x0 + tid] = s;
+        if (p.grad_w) p.grad_w[(size_t)bh * DK + x0 + tid] = w_;
+        if (p.grad_b && tid == 0 && rank == 0) {
             float b_ = 0.f;
-            for (int j = 0; j < TL; ++j) b_ += red2[TL * DK + j];
+            for (int j = 0; j < NW; ++j) b_ += red3[j];
             p.grad_b[bh] = b_;
         }
     }
@@ -701,9 +736,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT_R, 1)
 
 template <int DK, int DV>
 size_t fwd_smem() {
-    constexpr int TL = TL_F, NP = NT_F / 32;
-    return sizeof(float) *
-           (2 * (TL * (3 * DK + 2 * DV) + TL) + 3 * TL * NP * DK + 2 * TL * DK + TL * TL);
+    constexpr int TL = TL_F, NW = NT_F / 32, H2 = DK / 2;
+    return sizeof(float) * (2 * (TL * (3 * DK + 2 * DV) + TL) + 3 * TL * NW * H2 + TL * H2 +
+                            TL * DK + TL * TL + 2 * TL * 4);
 }
 template <int DK, int DV>
 size_t rev_smem() {
@@ -722,7 +757,7 @@ cudaError_t launch_shape(const BwdParams &p, cudaStream_t st) {
     e = cudaFuncSetAttribute(rev_sweep_kernel<DK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)rb);
     if (e != cudaSuccess) return e;
-    fwd_sweep_kernel<DK, DV><<<p.BH, NT_F, fb, st>>>(p);
+    fwd_sweep_kernel<DK, DV><<<2 * p.BH, NT_F, fb, st>>>(p);  // a CTA pair per (b, h)
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     rev_sweep_kernel<DK, DV><<<2 * p.BH, NT_R, rb, st>>>(p);  // a CTA pair per (b, h)
