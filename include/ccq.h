@@ -1,6 +1,7 @@
 /*
  * ccq.h -- C ABI of the CCQ (Curvature-Conditioned Query) linear-attention
- * forward for GB300 (sm_103a).
+ * read for GB300 (sm_103a): forward, single-token steps, the gradients of the
+ * GLA forward, and the key-covariance diagnostics.
  *
  * What the library computes (per batch b, head h, token t; S is d_k x d_v):
  *
