@@ -185,13 +185,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT_F, 1)
         //     S_u g_u of every token (one loaded k, q, v, g vector serves RX rows)
         for (int u = 0; u < n; ++u) {
             const float *qv = Q + u * DK, *kv = K + u * DK, *vv = V + u * DV, *gv = G + u * DV;
-            float kx[RX], ax[RX], a[RX], s[RX];
+            float kx[RX], ax[RX], a[RX], s[RX], a2[RX], s2[RX];
 #pragma unroll
             for (int i = 0; i < RX; ++i) {
                 kx[i] = kv[x0 + lane + 32 * i];
                 ax[i] = expf(LA[u * DK + x0 + lane + 32 * i]);
-                a[i] = 0.f;
-                s[i] = 0.f;
+                a[i] = a2[i] = 0.f;
+                s[i] = s2[i] = 0.f;
             }
 #pragma unroll
             for (int r = 0; r < CW; r += 4) {
@@ -203,9 +203,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT_F, 1)
                     Cr[i][r + 2] = fmaf(k4.z, kx[i], Cr[i][r + 2]);
                     Cr[i][r + 3] = fmaf(k4.w, kx[i], Cr[i][r + 3]);
                     a[i] = fmaf(Cr[i][r], q4.x, a[i]);
-                    a[i] = fmaf(Cr[i][r + 1], q4.y, a[i]);
+                    a2[i] = fmaf(Cr[i][r + 1], q4.y, a2[i]);
                     a[i] = fmaf(Cr[i][r + 2], q4.z, a[i]);
-                    a[i] = fmaf(Cr[i][r + 3], q4.w, a[i]);
+                    a2[i] = fmaf(Cr[i][r + 3], q4.w, a2[i]);
                 }
             }
 #pragma unroll
@@ -218,15 +218,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT_F, 1)
                     Sr[i][r + 2] = fmaf(ax[i], Sr[i][r + 2], kx[i] * v4.z);
                     Sr[i][r + 3] = fmaf(ax[i], Sr[i][r + 3], kx[i] * v4.w);
                     s[i] = fmaf(Sr[i][r], g4.x, s[i]);
-                    s[i] = fmaf(Sr[i][r + 1], g4.y, s[i]);
+                    s2[i] = fmaf(Sr[i][r + 1], g4.y, s2[i]);
                     s[i] = fmaf(Sr[i][r + 2], g4.z, s[i]);
-                    s[i] = fmaf(Sr[i][r + 3], g4.w, s[i]);
+                    s2[i] = fmaf(Sr[i][r + 3], g4.w, s2[i]);
                 }
             }
 #pragma unroll
             for (int i = 0; i < RX; ++i) {
-                red1[u * RED + warp * H2 + lane + 32 * i] = a[i];
-                red2[u * RED + warp * H2 + lane + 32 * i] = s[i];
+                red1[u * RED + warp * H2 + lane + 32 * i] = a[i] + a2[i];
+                red2[u * RED + warp * H2 + lane + 32 * i] = s[i] + s2[i];
             }
             if (warp == 0) {
 #pragma unroll
@@ -300,22 +300,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT_F, 1)
         //     k_u' . gy_u for u < u' (C_u = C_end - sum_{u'>u} k_u' k_u'^T),
         //     those pairs dealt round-robin over the warps
         for (int v_ = 0; v_ < n; ++v_) {
-            float a[RX];
+            float a[RX], a2[RX];
 #pragma unroll
-            for (int i = 0; i < RX; ++i) a[i] = 0.f;
+            for (int i = 0; i < RX; ++i) a[i] = a2[i] = 0.f;
 #pragma unroll
             for (int r = 0; r < CW; r += 4) {
                 const float4 y4 = ld4(gyb + v_ * DK + warp * CW + r);
 #pragma unroll
                 for (int i = 0; i < RX; ++i) {
                     a[i] = fmaf(Cr[i][r], y4.x, a[i]);
-                    a[i] = fmaf(Cr[i][r + 1], y4.y, a[i]);
+                    a2[i] = fmaf(Cr[i][r + 1], y4.y, a2[i]);
                     a[i] = fmaf(Cr[i][r + 2], y4.z, a[i]);
-                    a[i] = fmaf(Cr[i][r + 3], y4.w, a[i]);
+                    a2[i] = fmaf(Cr[i][r + 3], y4.w, a2[i]);
                 }
             }
 #pragma unroll
-            for (int i = 0; i < RX; ++i) red3[v_ * RED + warp * H2 + lane + 32 * i] = a[i];
+            for (int i = 0; i < RX; ++i) red3[v_ * RED + warp * H2 + lane + 32 * i] = a[i] + a2[i];
         }
         for (int pr = warp; pr < TL * (TL - 1) / 2; pr += NW) {
             int up = 1, uu = pr;
@@ -574,12 +574,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT_R, 1)
         for (int u = n - 1; u >= 0; --u) {
             const float rn = 1.0f / (float)(p.t0 + tc + u + 1);
             const float *qv = Q + u * DK, *yv = GY + u * DK, *kv = K + u * DK;
-            float gyn[RX], qn[RX], cc[RX];
+            float gyn[RX], qn[RX], cc[RX], cc2[RX];
 #pragma unroll
             for (int i = 0; i < RX; ++i) {
                 gyn[i] = yv[x0 + lane + 32 * i] * rn;
                 qn[i] = qv[x0 + lane + 32 * i] * rn;
-                cc[i] = 0.f;
+                cc[i] = cc2[i] = 0.f;
             }
 #pragma unroll
             for (int r = 0; r < CW; r += 4) {
@@ -592,13 +592,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NT_R, 1)
                     Gr[i][r + 2] = fmaf(gyn[i], q4.z, fmaf(qn[i], y4.z, Gr[i][r + 2]));
                     Gr[i][r + 3] = fmaf(gyn[i], q4.w, fmaf(qn[i], y4.w, Gr[i][r + 3]));
                     cc[i] = fmaf(Gr[i][r], k4.x, cc[i]);
-                    cc[i] = fmaf(Gr[i][r + 1], k4.y, cc[i]);
+                    cc2[i] = fmaf(Gr[i][r + 1], k4.y, cc2[i]);
                     cc[i] = fmaf(Gr[i][r + 2], k4.z, cc[i]);
-                    cc[i] = fmaf(Gr[i][r + 3], k4.w, cc[i]);
+                    cc2[i] = fmaf(Gr[i][r + 3], k4.w, cc2[i]);
                 }
             }
 #pragma unroll
-            for (int i = 0; i < RX; ++i) red_gk[u * RED + warp * H2 + lane + 32 * i] = cc[i];
+            for (int i = 0; i < RX; ++i) red_gk[u * RED + warp * H2 + lane + 32 * i] = cc[i] + cc2[i];
         }
         // (1d) the in-chunk pairs u <= u' (TL (TL + 1) / 2 of them), dealt
         //      round-robin over the warps (both CTAs form all of them)
