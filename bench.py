@@ -138,6 +138,24 @@ class ClockSampler:
         return out
 
 
+class L2Flush:
+    """Empties L2 between timed steps: writes a buffer of twice the L2 size
+    (every line of the working set is evicted), then reads another buffer of
+    twice the L2 size, so that the memset's dirty lines are written back
+    before the timed step starts rather than during it.  The step then starts
+    from a cold, clean L2."""
+
+    def __init__(self, dev):
+        prop = torch.cuda.get_device_properties(dev)
+        l2 = getattr(prop, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
+        self.write = torch.empty(int(2 * l2) // 4, dtype=torch.int32, device=dev)
+        self.read = torch.zeros(int(2 * l2) // 4, dtype=torch.int32, device=dev)
+
+    def __call__(self):
+        self.write.zero_()
+        return self.read.sum()
+
+
 def dist_setup(n_gpus: int):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -239,9 +257,7 @@ def run_ours(args, world, rank, local):
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     o = torch.empty_like(d["v"])
     stream = torch.cuda.current_stream()
-    prop = torch.cuda.get_device_properties(dev)
-    l2 = getattr(prop, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
-    flush = torch.empty(int(2 * l2) // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
 
     def step():
         if gdn:
@@ -264,7 +280,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         for i in range(args.steps):
-            flush.zero_()                       # L2 flush, outside the timed interval
+            flush()                       # L2 flush, outside the timed interval
             ev[i][0].record(stream)
             step()
             ev[i][1].record(stream)
@@ -346,7 +362,8 @@ def run_ours(args, world, rank, local):
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "T": w.T, "dk": w.dk, "dv": w.dv,
-                   "state": "fp32", "l2": "flushed (2x L2 memset) before every timed step; "
+                   "state": "fp32", "l2": "flushed (2x L2 memset, then a 2x L2 read: no dirty "
+                                         "line left) before every timed step; "
                                          "inputs 268 MB > L2",
                    "parallelism": f"replicas x{world}"},
         "tflops": tflops,
@@ -381,9 +398,7 @@ def run_overhead(args, world, rank, local):
     B, H, d = 4, 16, 128
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
-    prop = torch.cuda.get_device_properties(dev)
-    l2 = getattr(prop, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
-    flush = torch.empty(int(2 * l2) // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
     g = torch.Generator(device=dev).manual_seed(2)
     wl = torch.randn((H, d), generator=g, device=dev) / d ** 0.5
     bl = torch.zeros(H, device=dev)
@@ -410,7 +425,7 @@ def run_overhead(args, world, rank, local):
                     fwd()
                 ts = []
                 for _ in range(args.steps):
-                    flush.zero_()
+                    flush()
                     e0 = torch.cuda.Event(enable_timing=True)
                     e1 = torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
@@ -437,7 +452,8 @@ def run_overhead(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (drawn on the device)",
         "config": {"workload": "gla_bf16_b4h16d128_tsweep", "B": B, "H": H, "dk": d, "dv": d,
                    "T": [r["T"] for r in rows],
-                   "l2": "flushed (2x L2 memset) before every timed forward; median of steps"},
+                   "l2": "flushed (2x L2 memset, then a 2x L2 read) before every timed "
+                         "forward; median of steps"},
         "sweep": rows, "gpu_launches": 2 * len(rows) * args.steps, "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -683,9 +699,7 @@ def run_step(args, world, rank, local):
     m = K0.sum(2).contiguous().to(dev)
     o = torch.empty((B, H, d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
-    prop = torch.cuda.get_device_properties(dev)
-    l2 = getattr(prop, "L2_cache_size", 126 * 2 ** 20) or 126 * 2 ** 20
-    flush = torch.empty(int(2 * l2) // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
     t_seen = [4096]
 
     def step(tok):
@@ -708,7 +722,7 @@ def run_step(args, world, rank, local):
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
         for i in range(args.steps):
-            flush.zero_()                       # the state (269 MB) is larger than L2 anyway
+            flush()                       # the state (269 MB) is larger than L2 anyway
             ev[i][0].record(stream)
             step(toks[args.warmup + i])
             ev[i][1].record(stream)
@@ -779,7 +793,8 @@ def run_step(args, world, rank, local):
         "data": "synthetic",
         "config": {"workload": w.name, "B": B, "H": H, "dk": d, "dv": d, "inputs": "bf16",
                    "state": "fp32, resident, updated in place",
-                   "l2": "flushed (2x L2 memset) before every timed step; state 269 MB > L2",
+                   "l2": "flushed (2x L2 memset, then a 2x L2 read) before every timed "
+                         "step; state 269 MB > L2",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": None,
