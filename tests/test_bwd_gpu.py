@@ -144,3 +144,27 @@ def test_workspace_too_small_is_rejected():
         ccq.gla_bwd(d["q"], d["k"], d["v"], d["log_alpha"], d["w_lambda"], d["b_lambda"],
                     d["grad_o"], workspace=small)
     assert e.value.code == 1
+
+
+@pytest.mark.parametrize("T", [8, 9, 16])
+def test_chunk_boundaries(T):
+    """T at a chunk multiple and one past it (chunks of 8 tokens)."""
+    inp, extra = _case(128, 64, T, seed=40 + T, state=True, up=True)
+    _compare(_run(inp, extra, True), _oracle(inp, extra), 2e-4, state=True)
+
+
+def test_many_heads_given_lambda_with_state():
+    """B3 H5: fifteen CTA pairs; a given lambda, carried state and state
+    gradients together, d_k = 64, d_v = 128."""
+    inp, extra = _case(64, 128, 23, B=3, H=5, seed=50, state=True, lam=True, up=True)
+    _compare(_run(inp, extra, True), _oracle(inp, extra), 2e-4, state=True)
+
+
+def test_strong_decay():
+    """log alpha about -5 per token and channel: the decay products across a
+    chunk underflow; the sweeps only ever form exp of non-positive
+    differences, so nothing divides by a vanishing product."""
+    inp, extra = _case(128, 128, 40, seed=60)
+    inp["log_alpha"] = (inp["log_alpha"] * 80.0).clamp(min=-12.0)
+    assert inp["log_alpha"].min().item() < -8.0
+    _compare(_run(inp, extra), _oracle(inp, extra), 2e-4)
