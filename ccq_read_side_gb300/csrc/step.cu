@@ -129,7 +129,8 @@ ccq_step_kernel(const __grid_constant__ StepParams p) {
         qv[i] = ld1(q, i);
         kv[i] = ld1(k, i);
         mv[i] = m[i];
-        if (!GDN) av[i] = ld1(static_cast<const TIn *>(p.log_alpha), (size_t)bh * DK + i);
+        // alpha itself (one exp per channel, not per state element)
+        if (!GDN) av[i] = expf(ld1(static_cast<const TIn *>(p.log_alpha), (size_t)bh * DK + i));
     }
     for (int i = tid; i < DV; i += NTHREADS) vv[i] = ld1(v, i);
     __syncthreads();  // barrier initialised, vectors in place
@@ -204,7 +205,7 @@ ccq_step_kernel(const __grid_constant__ StepParams p) {
         if (GDN)
             s = alpha_s * (s - beta_s * kc * upart[j]) + beta_s * kc * vv[j];
         else
-            s = expf(av[r0 + c]) * s + kc * vv[j];
+            s = av[r0 + c] * s + kc * vv[j];
         sS[c][j] = s;
     }
     for (int i = tid; i < R * DK; i += NTHREADS) {
