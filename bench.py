@@ -332,14 +332,23 @@ def run_ours(args, world, rank, local):
     keys = ("q", "k", "v", "log_alpha", "w_lambda", "b_lambda") + (("beta",) if gdn else ())
     h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
     d2h = o_host.numel() * o_host.element_size()
+    staging = None
+    if not gdn:  # the C ABI's host-buffer entry point: copies, forward, copy back
+        staging = torch.empty(ccq.gla_fwd_host_staging_bytes(w.B, w.H, w.T, w.dk, w.dv,
+                                                             d["q"].dtype),
+                              dtype=torch.uint8, device=dev)
 
-    # each input's copy on its own stream (several copy engines at once); the
-    # copies of a step start after the previous step's work has been enqueued
-    # and the forward waits for all of them
-    side = [torch.cuda.Stream(device=dev) for _ in keys]
-    dbuf = {k: torch.empty(host[k].shape, dtype=host[k].dtype, device=dev) for k in keys}
+    # GLA: ccq_gla_fwd_host (one copy per input on the stream, the forward, the
+    # copy back).  Gated DeltaNet: each input's copy on its own stream (several
+    # copy engines at once), the forward waiting for all of them
+    side = [torch.cuda.Stream(device=dev) for _ in keys] if gdn else []
+    dbuf = {k: torch.empty(host[k].shape, dtype=host[k].dtype, device=dev) for k in keys} if gdn \
+        else {}
 
     def e2e_step():
+        if not gdn:
+            ccq.gla_fwd_host(*(host[k] for k in keys), o=o_host, staging=staging, stream=stream)
+            return
         start = torch.cuda.Event()
         start.record(stream)
         for s_, k in zip(side, keys):
@@ -349,13 +358,9 @@ def run_ours(args, world, rank, local):
             done = torch.cuda.Event()
             done.record(s_)
             stream.wait_event(done)
-        dd = dbuf
-        if gdn:
-            oo, _ = ccq.gdn_fwd(dd["q"], dd["k"], dd["v"], dd["log_alpha"], dd["beta"],
-                                dd["w_lambda"], dd["b_lambda"], want_state=False, stream=stream)
-        else:
-            oo, _ = ccq.gla_fwd(dd["q"], dd["k"], dd["v"], dd["log_alpha"], dd["w_lambda"],
-                                dd["b_lambda"], want_state=False, stream=stream)
+        dd = dbuf  # Gated DeltaNet: device copies made here, then the device-pointer call
+        oo, _ = ccq.gdn_fwd(dd["q"], dd["k"], dd["v"], dd["log_alpha"], dd["beta"],
+                            dd["w_lambda"], dd["b_lambda"], want_state=False, stream=stream)
         o_host.copy_(oo, non_blocking=True)
 
     for _ in range(max(1, min(args.warmup, 3))):

@@ -16,7 +16,7 @@ from typing import Dict, Optional, Tuple
 
 import torch
 
-__all__ = ["gla_fwd", "gdn_fwd", "gla_step", "gdn_step", "gla_bwd", "gla_bwd_workspace_bytes",
+__all__ = ["gla_fwd", "gla_fwd_host", "gla_fwd_host_staging_bytes", "gdn_fwd", "gla_step", "gdn_step", "gla_bwd", "gla_bwd_workspace_bytes",
            "sigma_subspace", "subspace_alignment", "last_device_status", "status_string", "CcqError",
            "library", "FLAG_L2NORM_QK", "FLAG_FP32_PATH", "FLAG_PLAIN_GLA", "FLAG_TEST_STALL",
            "STATUS"]
@@ -70,6 +70,10 @@ def library() -> ctypes.CDLL:
     lib.ccq_gla_bwd.restype = I
     lib.ccq_gla_bwd.argtypes = ([P] * 10 + [ctypes.c_int64] + [P] * 14 + [ctypes.c_size_t]
                                 + [I] * 5 + [ctypes.c_uint, P])
+    lib.ccq_gla_fwd_host_staging_bytes.restype = ctypes.c_size_t
+    lib.ccq_gla_fwd_host_staging_bytes.argtypes = [I, I, I, I, I, I]
+    lib.ccq_gla_fwd_host.restype = I
+    lib.ccq_gla_fwd_host.argtypes = [P] * 8 + [ctypes.c_size_t] + [I] * 6 + [ctypes.c_uint, P]
     lib.ccq_gla_bwd_noalloc.restype = I
     lib.ccq_gla_bwd_noalloc.argtypes = ([P] * 10 + [ctypes.c_int64] + [P] * 13 + [I] * 5
                                         + [ctypes.c_uint, P])
@@ -174,6 +178,50 @@ def gla_fwd(q, k, v, log_alpha, w_lambda=None, b_lambda=None, *, lambda_in=None,
     Asynchronous on `stream` (default: torch's current stream)."""
     return _fwd("gla", q, k, v, log_alpha, None, w_lambda, b_lambda, lambda_in, S0, C0, m0, t0,
                 o, lambda_out, want_state, chunk, flags, stream)
+
+
+def gla_fwd_host_staging_bytes(B: int, H: int, T: int, dk: int, dv: int, dtype) -> int:
+    """Bytes of device staging ccq_gla_fwd_host needs for these sizes."""
+    return int(library().ccq_gla_fwd_host_staging_bytes(B, H, T, dk, dv, _DTYPES[dtype]))
+
+
+def gla_fwd_host(q, k, v, log_alpha, w_lambda, b_lambda, *, o=None, staging=None,
+                 device=None, flags: int = 0, stream=None) -> torch.Tensor:
+    """CCQ-GLA forward from host (CPU) tensors through ccq_gla_fwd_host: the
+    library copies the inputs into `staging` (a CUDA tensor of at least
+    gla_fwd_host_staging_bytes(...) bytes, allocated here when None), runs the
+    forward and copies o back into the host tensor `o` (allocated pinned when
+    None).  Asynchronous on `stream`: o is valid after the stream synchronises.
+    Zero initial state, no state outputs."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = q.dtype
+    if dt not in _DTYPES:
+        raise ValueError(f"unsupported dtype {dt}")
+    for name, t, shp, tdt in (("q", q, (B, H, T, dk), dt), ("k", k, (B, H, T, dk), dt),
+                              ("v", v, (B, H, T, dv), dt),
+                              ("log_alpha", log_alpha, (B, H, T, dk), dt),
+                              ("w_lambda", w_lambda, (H, dk), torch.float32),
+                              ("b_lambda", b_lambda, (H,), torch.float32)):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != tdt or tuple(t.shape) != shp:
+            raise ValueError(f"{name} must be a contiguous host tensor {tdt} {shp}")
+    if o is None:
+        o = torch.empty((B, H, T, dv), dtype=dt).pin_memory()
+    if o.is_cuda or not o.is_contiguous() or o.dtype != dt or tuple(o.shape) != (B, H, T, dv):
+        raise ValueError("o must be a contiguous host tensor like v")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    need = gla_fwd_host_staging_bytes(B, H, T, dk, dv, dt)
+    if staging is None:
+        staging = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _need(staging, "staging", None, None, dev)
+    with torch.cuda.device(dev):
+        rc = library().ccq_gla_fwd_host(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(w_lambda), _ptr(b_lambda), _ptr(o),
+            _ptr(staging), staging.numel() * staging.element_size(), B, H, T, dk, dv,
+            _DTYPES[dt], int(flags), _stream(stream))
+    if rc != 0:
+        raise CcqError(rc, "ccq_gla_fwd_host")
+    return o
 
 
 def gdn_fwd(q, k, v, log_alpha, beta, w_lambda=None, b_lambda=None, *, lambda_in=None, S0=None,

@@ -225,6 +225,69 @@ extern "C" ccq_status ccq_subspace_alignment(const float *U, const void *X, int 
                                       reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Device staging for ccq_gla_fwd_host: q, k, log_alpha, v, o, w_lambda,
+// b_lambda, each at a 256-byte boundary.
+struct HostStaging {
+    size_t q, k, la, v, o, w, b, total;
+    HostStaging(long long BH, long long T, int dk, int dv, int H, size_t elem) {
+        auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+        size_t at = 0;
+        q = at, at += up(BH * T * dk * elem);
+        k = at, at += up(BH * T * dk * elem);
+        la = at, at += up(BH * T * dk * elem);
+        v = at, at += up(BH * T * dv * elem);
+        o = at, at += up(BH * T * dv * elem);
+        w = at, at += up((size_t)H * dk * sizeof(float));
+        b = at, at += up((size_t)H * sizeof(float));
+        total = at;
+    }
+};
+
+extern "C" size_t ccq_gla_fwd_host_staging_bytes(int B, int H, int T, int dk, int dv,
+                                                 ccq_dtype dtype) {
+    if (B < 0 || H < 0 || T < 0 || dk < 1 || dv < 1) return 0;
+    if (dtype != CCQ_DTYPE_F32 && dtype != CCQ_DTYPE_BF16) return 0;
+    return HostStaging((long long)B * H, T, dk, dv, H, dtype == CCQ_DTYPE_BF16 ? 2 : 4).total;
+}
+
+extern "C" ccq_status ccq_gla_fwd_host(const void *q, const void *k, const void *v,
+                                       const void *log_alpha, const float *w_lambda,
+                                       const float *b_lambda, void *o, void *staging,
+                                       size_t staging_bytes, int B, int H, int T, int dk,
+                                       int dv, ccq_dtype dtype, unsigned flags,
+                                       ccq_stream_t stream) {
+    if (B < 0 || H < 0 || T < 0) return CCQ_ERR_INVALID_ARG;
+    if (dtype != CCQ_DTYPE_F32 && dtype != CCQ_DTYPE_BF16) return CCQ_ERR_UNSUPPORTED;
+    if (flags & ~(CCQ_FLAG_L2NORM_QK | CCQ_FLAG_FP32_PATH)) return CCQ_ERR_INVALID_ARG;
+    const long long BH = (long long)B * H;
+    if (BH == 0 || T == 0) return CCQ_OK;  // nothing to copy or compute
+    if (!q || !k || !v || !log_alpha || !w_lambda || !b_lambda || !o || !staging)
+        return CCQ_ERR_INVALID_ARG;
+    if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return CCQ_ERR_UNSUPPORTED;
+    const size_t elem = dtype == CCQ_DTYPE_BF16 ? 2 : 4;
+    const HostStaging L(BH, T, dk, dv, H, elem);
+    if (staging_bytes < L.total || ((uintptr_t)staging & 255u)) return CCQ_ERR_INVALID_ARG;
+    char *d = static_cast<char *>(staging);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const size_t nk = (size_t)BH * T * dk * elem, nv = (size_t)BH * T * dv * elem;
+    // one copy per tensor, in stream order
+    const struct { size_t off; const void *src; size_t bytes; } in[] = {
+        {L.q, q, nk}, {L.k, k, nk}, {L.la, log_alpha, nk}, {L.v, v, nv},
+        {L.w, w_lambda, (size_t)H * dk * sizeof(float)}, {L.b, b_lambda, (size_t)H * sizeof(float)}};
+    for (const auto &c : in)
+        if (cudaMemcpyAsync(d + c.off, c.src, c.bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+            return CCQ_ERR_CUDA;
+    const ccq_status s = ccq_gla_fwd(d + L.q, d + L.k, d + L.v, d + L.la,
+                                     reinterpret_cast<const float *>(d + L.w),
+                                     reinterpret_cast<const float *>(d + L.b), nullptr, nullptr,
+                                     d + L.o, nullptr, nullptr, nullptr, 0, nullptr, nullptr,
+                                     nullptr, B, H, T, dk, dv, 0, dtype, flags, stream);
+    if (s != CCQ_OK) return s;
+    if (cudaMemcpyAsync(o, d + L.o, nv, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return CCQ_ERR_CUDA;
+    return CCQ_OK;
+}
+
 extern "C" size_t ccq_gla_bwd_workspace_bytes(int B, int H, int T, int dk, int dv) {
     (void)dv;
     if (B < 0 || H < 0 || T < 0 || dk < 1) return 0;

@@ -128,6 +128,26 @@ ccq_status ccq_gdn_fwd(const void *q, const void *k, const void *v, const void *
                        int chunk, ccq_dtype dtype, unsigned flags, ccq_stream_t stream);
 
 /*
+ * ccq_gla_fwd from HOST buffers: q, k, v, log_alpha, o (layouts and dtype as
+ * ccq_gla_fwd) and w_lambda [H, dk], b_lambda [H] (float32) are host memory;
+ * page-locked memory makes the copies asynchronous, pageable memory works but
+ * the copies then wait for the host.  The call enqueues on `stream`: one
+ * cudaMemcpyAsync per input into `staging`, the forward on the staged copies
+ * (zero initial state, no state, lambda or statistics outputs), and one copy
+ * of o back into the host buffer; o is valid once the stream has reached
+ * that point.  staging: device memory of at least
+ * ccq_gla_fwd_host_staging_bytes(B, H, T, dk, dv, dtype) bytes, 256-byte
+ * aligned, owned by the caller and overwritten; the library allocates
+ * nothing.  flags: CCQ_FLAG_L2NORM_QK, CCQ_FLAG_FP32_PATH.  An empty batch
+ * or T = 0 returns CCQ_OK without any CUDA call.  Errors as ccq_gla_fwd.
+ */
+size_t ccq_gla_fwd_host_staging_bytes(int B, int H, int T, int dk, int dv, ccq_dtype dtype);
+ccq_status ccq_gla_fwd_host(const void *q, const void *k, const void *v, const void *log_alpha,
+                            const float *w_lambda, const float *b_lambda, void *o,
+                            void *staging, size_t staging_bytes, int B, int H, int T, int dk,
+                            int dv, ccq_dtype dtype, unsigned flags, ccq_stream_t stream);
+
+/*
  * Single-token step (decode) on the GLA backbone: one new token per (b, h)
  * read against a carried state, which is updated in place.  Same operator as
  * ccq_gla_fwd with T = 1 (the read uses the state after this token's write);

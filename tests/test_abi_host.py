@@ -193,3 +193,23 @@ def test_backward_workspace_size(lib):
 ])
 def test_backward_validates_synchronously(lib, case, code):
     assert _bwd(lib, **case) == code
+
+
+def test_host_forward_validates_synchronously(lib):
+    n = lib.ccq_gla_fwd_host_staging_bytes(1, 2, 10, 64, 64, 1)
+    assert n >= 5 * 2 * 10 * 64 * 2 and n % 256 == 0
+    assert lib.ccq_gla_fwd_host_staging_bytes(1, 2, 10, 64, 64, 7) == 0
+    args = dict(q=FAKE, k=FAKE, v=FAKE, la=FAKE, w=FAKE, b=FAKE, o=FAKE, st=FAKE, st_bytes=1 << 40,
+                B=1, H=2, T=10, dk=64, dv=64, dtype=1, flags=0, stream=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return lib.ccq_gla_fwd_host(*a.values())
+
+    assert call(st=None) == 1                         # staging required
+    assert call(st_bytes=16) == 1                      # staging too small
+    assert call(st=ctypes.c_void_p(0x1010)) == 1       # staging 256-byte aligned
+    assert call(dk=96) == 2
+    assert call(flags=4) == 1                          # only L2-norm and the fp32 path
+    assert call(B=0, q=None, k=None, v=None, la=None, w=None, b=None, o=None, st=None) == 0

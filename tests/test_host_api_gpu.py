@@ -1,0 +1,40 @@
+"""ccq_gla_fwd_host (host buffers, copies inside the call) against
+ccq_gla_fwd on device buffers: the same kernels on the same values, so the
+outputs are bit-identical."""
+import pytest
+import torch
+
+import ccq_read_side_gb300 as ccq
+from ccq_read_side_gb300.workloads import Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dtype,d,pinned", [("bf16", 128, True), ("bf16", 128, False),
+                                            ("f32", 64, True)])
+def test_host_forward_equals_device_forward(dtype, d, pinned):
+    w = Workload("host", "gla", dtype, 1, 3, 203, d, d, 64, 21, "iso")
+    inp = make_inputs(w)
+    keys = ("q", "k", "v", "log_alpha", "w_lambda", "b_lambda")
+    host = {k: (inp[k].pin_memory() if pinned else inp[k].contiguous()) for k in keys}
+    o_host = ccq.gla_fwd_host(*(host[k] for k in keys))
+    torch.cuda.synchronize()
+    dev = {k: inp[k].cuda() for k in keys}
+    o_dev, _ = ccq.gla_fwd(*(dev[k] for k in keys), want_state=False)
+    torch.cuda.synchronize()
+    assert ccq.last_device_status() == 0
+    assert torch.equal(o_host, o_dev.cpu())
+
+
+def test_host_forward_twice_with_one_staging_buffer():
+    w = Workload("host2", "gla", "bf16", 2, 2, 130, 128, 128, 64, 22, "iso")
+    keys = ("q", "k", "v", "log_alpha", "w_lambda", "b_lambda")
+    staging = torch.empty(ccq.gla_fwd_host_staging_bytes(2, 2, 130, 128, 128, torch.bfloat16),
+                          dtype=torch.uint8, device="cuda")
+    for seed in (1, 2):
+        inp = make_inputs(w, seed=seed)
+        o_host = ccq.gla_fwd_host(*(inp[k].pin_memory() for k in keys), staging=staging)
+        torch.cuda.synchronize()
+        o_dev, _ = ccq.gla_fwd(*(inp[k].cuda() for k in keys), want_state=False)
+        torch.cuda.synchronize()
+        assert torch.equal(o_host, o_dev.cpu())
