@@ -305,7 +305,8 @@ extern "C" ccq_status ccq_gla_bwd(
     if (B < 0 || H < 0 || T < 0 || t0 < 0) return CCQ_ERR_INVALID_ARG;
     if ((dk != 64 && dk != 128) || (dv != 64 && dv != 128)) return CCQ_ERR_UNSUPPORTED;
     if (flags != 0) return CCQ_ERR_INVALID_ARG;
-    if ((long long)B * H > 0x7fffffffLL || (long long)T + t0 > (1LL << 40))
+    // a CTA pair per (b, h): the grid of 2 B H CTAs must fit an int
+    if ((long long)B * H > (1LL << 30) || (long long)T + t0 > (1LL << 40))
         return CCQ_ERR_UNSUPPORTED;
     const int given = (S0 != nullptr) + (C0 != nullptr) + (m0 != nullptr);
     if (given != 0 && given != 3) return CCQ_ERR_INVALID_ARG;

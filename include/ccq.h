@@ -216,10 +216,10 @@ ccq_status ccq_subspace_alignment(const float *U, const void *X, int BH, int dk,
  *     k k^T; only the symmetric part of grad_C matters, and C0 must be
  *     symmetric).
  * Inputs as ccq_gla_fwd (float32; q, k, v, log_alpha, grad_o 16-byte
- * aligned); grad_S, grad_C, grad_m nullable (zero).  The gradients are those
- * of the forward's definition (the read after the write; Sigma_t with n_t =
- * t0 + t + 1); the method's pages describe the forward only, the backward is
- * its derivative.
+ * aligned; B * H <= 2^30); grad_S, grad_C, grad_m nullable (zero).  The
+ * gradients are those of the forward's definition (the read after the write;
+ * Sigma_t with n_t = t0 + t + 1); the method's pages describe the forward
+ * only, the backward is its derivative.
  * workspace: device memory of at least ccq_gla_bwd_workspace_bytes(B, H, T,
  * dk, dv) bytes (3 dk + 4 floats per token and head, plus dk per head),
  * 16-byte aligned, owned by the caller, overwritten.  Two kernels run in

@@ -189,6 +189,7 @@ def test_backward_workspace_size(lib):
     (dict(w=None), 1),                             # the gate needs w and b ...
     (dict(w=None, b=None, lin=FAKE, ws=None), 1),  # ... unless lambda is given
     (dict(gq=None), 1),
+    (dict(B=1 << 16, H=1 << 15), 2),               # 2 B H CTAs would not fit the grid
     (dict(B=0, q=None, k=None, v=None, la=None, go=None, ws=None), 0),  # empty batch: no CUDA call
 ])
 def test_backward_validates_synchronously(lib, case, code):
