@@ -10,7 +10,7 @@ import torch
 import ccq_read_side_gb300 as ccq
 import oracle
 from ccq_read_side_gb300.workloads import WORKLOADS, Workload, make_inputs
-from parity import TOL_BF16, check, check_all, np64, run_both, to_dev
+from parity import check, check_all, np64, run_both, to_dev
 
 pytestmark = pytest.mark.gpu
 
