@@ -68,17 +68,20 @@ sigma_subspace_kernel(const float *__restrict__ C, const float *__restrict__ m, 
             G[a * KMAX + b] = s;
         }
         __syncthreads();
-        if (tid == 0) {  // Cholesky, upper factor R in place (k <= 32: one thread)
+        if (tid < 32) {  // Cholesky, upper factor R in place; warp 0, lane b owns column b
+            const int b = tid;
             for (int a = 0; a < k; ++a) {
-                float d = G[a * KMAX + a];
+                float d = G[a * KMAX + a];  // every lane forms the pivot (same reads)
                 for (int l = 0; l < a; ++l) d -= G[l * KMAX + a] * G[l * KMAX + a];
                 d = sqrtf(fmaxf(d, 1e-30f));
-                G[a * KMAX + a] = d;
-                for (int b = a + 1; b < k; ++b) {
+                if (b > a && b < k) {
                     float s = G[a * KMAX + b];
                     for (int l = 0; l < a; ++l) s -= G[l * KMAX + a] * G[l * KMAX + b];
                     G[a * KMAX + b] = s / d;
                 }
+                __syncwarp();
+                if (b == a) G[a * KMAX + a] = d;
+                __syncwarp();
             }
         }
         __syncthreads();
@@ -113,43 +116,50 @@ sigma_subspace_kernel(const float *__restrict__ C, const float *__restrict__ m, 
         Q[a * KMAX + b] = a == b ? 1.f : 0.f;
     }
     __syncthreads();
-    if (tid == 0) {
-        for (int a = 0; a < k; ++a)  // symmetrise
-            for (int b = a + 1; b < k; ++b) {
-                const float s = 0.5f * (G[a * KMAX + b] + G[b * KMAX + a]);
-                G[a * KMAX + b] = G[b * KMAX + a] = s;
-            }
+    if (tid < 32) {  // warp 0: lane l owns row / column l of each rotation's update
+        const int l = tid;
+        if (l == 0)
+            for (int a = 0; a < k; ++a)  // symmetrise
+                for (int b = a + 1; b < k; ++b) {
+                    const float s = 0.5f * (G[a * KMAX + b] + G[b * KMAX + a]);
+                    G[a * KMAX + b] = G[b * KMAX + a] = s;
+                }
+        __syncwarp();
         for (int sweep = 0; sweep < 30; ++sweep) {
-            float off = 0.f;
+            float off = 0.f;  // every lane forms the same sum (same reads, same order)
             for (int a = 0; a < k; ++a)
                 for (int b = a + 1; b < k; ++b) off += G[a * KMAX + b] * G[a * KMAX + b];
             if (off < 1e-20f) break;
             for (int a = 0; a < k; ++a)
                 for (int b = a + 1; b < k; ++b) {
                     const float hab = G[a * KMAX + b];
-                    if (fabsf(hab) < 1e-30f) continue;
+                    if (fabsf(hab) < 1e-30f) continue;  // warp-uniform
                     // plane rotation J (c, s) with (J^T H J)[a][b] = 0: the classical
                     // cyclic Jacobi method for symmetric matrices
                     const float tau = (G[b * KMAX + b] - G[a * KMAX + a]) / (2.f * hab);
                     const float t = (tau >= 0.f ? 1.f : -1.f) / (fabsf(tau) + sqrtf(1.f + tau * tau));
                     const float c = 1.f / sqrtf(1.f + t * t), s = t * c;
-                    for (int l = 0; l < k; ++l) {  // H <- J^T H J
+                    __syncwarp();  // every lane has read this rotation's inputs
+                    if (l < k) {  // H <- H J: columns a and b, row l
                         const float x = G[l * KMAX + a], y = G[l * KMAX + b];
                         G[l * KMAX + a] = c * x - s * y;
                         G[l * KMAX + b] = s * x + c * y;
                     }
-                    for (int l = 0; l < k; ++l) {
+                    __syncwarp();
+                    if (l < k) {  // H <- J^T H: rows a and b, column l
                         const float x = G[a * KMAX + l], y = G[b * KMAX + l];
                         G[a * KMAX + l] = c * x - s * y;
                         G[b * KMAX + l] = s * x + c * y;
+                        const float qx = Q[l * KMAX + a], qy = Q[l * KMAX + b];  // Q <- Q J
+                        Q[l * KMAX + a] = c * qx - s * qy;
+                        Q[l * KMAX + b] = s * qx + c * qy;
                     }
-                    for (int l = 0; l < k; ++l) {  // Q <- Q J
-                        const float x = Q[l * KMAX + a], y = Q[l * KMAX + b];
-                        Q[l * KMAX + a] = c * x - s * y;
-                        Q[l * KMAX + b] = s * x + c * y;
-                    }
+                    __syncwarp();
                 }
         }
+    }
+    __syncthreads();
+    if (tid == 0) {
         // order by Ritz value, descending: a permutation stored in row 0 of Wm
         for (int a = 0; a < k; ++a) Wm[a] = (float)a;
         for (int a = 0; a < k; ++a)
