@@ -32,8 +32,26 @@ def _declared():
 def test_header_declares_the_entry_points():
     d = _declared()
     for n in ("ccq_gla_fwd", "ccq_gdn_fwd", "ccq_gla_step", "ccq_gdn_step", "ccq_status_string",
-              "ccq_last_device_status"):
+              "ccq_last_device_status", "ccq_gla_fwd_host", "ccq_gla_fwd_host_staging_bytes",
+              "ccq_gla_bwd", "ccq_gla_bwd_workspace_bytes", "ccq_gla_bwd_noalloc",
+              "ccq_sigma_subspace", "ccq_subspace_alignment"):
         assert n in d
+
+
+def test_header_is_plain_c(tmp_path):
+    """The ABI header compiles as strict C99 (no C++ or CUDA types in it)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "ccq.h"\n'
+                   "size_t f(void) { return ccq_gla_bwd_workspace_bytes(1, 1, 1, 64, 64); }\n")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-fsyntax-only", "-I", os.path.join(ROOT, "include"), str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
 
 
 def test_every_declared_symbol_is_exported(lib):
