@@ -28,7 +28,8 @@ template <int DK>
 __global__ void __launch_bounds__(NTHREADS)
 sigma_subspace_kernel(const float *__restrict__ C, const float *__restrict__ m, double n, int k,
                       int iters, float *__restrict__ U, float *__restrict__ ritz) {
-    extern __shared__ float sm[];
+    extern __shared__ float4 sm_f4[];  // 16-byte aligned (float2 / float4 reads below)
+    float *sm = reinterpret_cast<float *>(sm_f4);
     float *Sig = sm;                    // [DK][DK]
     float *V = Sig + DK * DK;           // [DK][KMAX]
     float *Wm = V + DK * KMAX;          // [DK][KMAX]
@@ -52,12 +53,31 @@ sigma_subspace_kernel(const float *__restrict__ C, const float *__restrict__ m, 
     }
     __syncthreads();
 
-    auto matmul_sigma = [&]() {  // Wm = Sig V
-        for (int x = tid; x < DK * k; x += NTHREADS) {
-            const int i = x / k, j = x % k;
-            float s = 0.f;
-            for (int l = 0; l < DK; ++l) s += Sig[i * DK + l] * V[l * KMAX + j];
-            Wm[i * KMAX + j] = s;
+    // Wm = Sig V.  A thread forms a 2-row x 4-column block; Sig is symmetric,
+    // so rows i0, i0+1 are read as column entries Sig[l][i0..i0+1] (one float2,
+    // consecutive across lanes) and V[l][j0..j0+3] as one float4.
+    auto matmul_sigma = [&]() {
+        const int kq = (k + 3) / 4;
+        for (int blk = tid; blk < (DK / 2) * kq; blk += NTHREADS) {
+            const int i0 = 2 * (blk / kq), j0 = 4 * (blk % kq);
+            float a[2][4] = {};
+            for (int l = 0; l < DK; ++l) {
+                const float2 sg = *reinterpret_cast<const float2 *>(&Sig[l * DK + i0]);
+                const float4 v4 = *reinterpret_cast<const float4 *>(&V[l * KMAX + j0]);
+                a[0][0] = fmaf(sg.x, v4.x, a[0][0]);
+                a[0][1] = fmaf(sg.x, v4.y, a[0][1]);
+                a[0][2] = fmaf(sg.x, v4.z, a[0][2]);
+                a[0][3] = fmaf(sg.x, v4.w, a[0][3]);
+                a[1][0] = fmaf(sg.y, v4.x, a[1][0]);
+                a[1][1] = fmaf(sg.y, v4.y, a[1][1]);
+                a[1][2] = fmaf(sg.y, v4.z, a[1][2]);
+                a[1][3] = fmaf(sg.y, v4.w, a[1][3]);
+            }
+#pragma unroll
+            for (int r = 0; r < 2; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (j0 + c < k) Wm[(i0 + r) * KMAX + j0 + c] = a[r][c];
         }
     };
     auto cholqr = [&]() {  // V = Wm R^-1, R^T R = Wm^T Wm
