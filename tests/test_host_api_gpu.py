@@ -38,3 +38,18 @@ def test_host_forward_twice_with_one_staging_buffer():
         o_dev, _ = ccq.gla_fwd(*(inp[k].cuda() for k in keys), want_state=False)
         torch.cuda.synchronize()
         assert torch.equal(o_host, o_dev.cpu())
+
+
+def test_host_forward_with_fused_l2_norm():
+    """The L2-normalisation flag routes the host call to the fp32 CUDA-core
+    kernel, exactly as the device call with the same flag."""
+    w = Workload("host3", "gla", "bf16", 1, 2, 77, 64, 128, 64, 23, "iso")
+    inp = make_inputs(w)
+    keys = ("q", "k", "v", "log_alpha", "w_lambda", "b_lambda")
+    inp["q"] = (inp["q"].float() * 3.0).to(torch.bfloat16)  # not unit norm: the flag matters
+    o_host = ccq.gla_fwd_host(*(inp[k].pin_memory() for k in keys), flags=ccq.FLAG_L2NORM_QK)
+    torch.cuda.synchronize()
+    o_dev, _ = ccq.gla_fwd(*(inp[k].cuda() for k in keys), want_state=False,
+                           flags=ccq.FLAG_L2NORM_QK)
+    torch.cuda.synchronize()
+    assert torch.equal(o_host, o_dev.cpu())
